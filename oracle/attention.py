@@ -1,0 +1,196 @@
+"""Plain fp64 definition of exact scaled-dot-product attention. TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU arms import this file.
+Source key ([MG-A], [MG-B], [AUT], [IMR], [PW]) is spelled out in
+``oracle/__init__.py``; each function names the passage it follows.
+
+Readings taken where the pages are silent (each one is listed with its reason
+in the design notes):
+  * the score scale is applied before the mask; masked scores are -inf;
+  * causal with Nq != Nk aligns the last query with the last key: query i sees
+    key j iff j <= i + (Nk - Nq) (equal to the pages' j <= i when Nq == Nk);
+  * a query row that sees no key has O = 0 and LSE = -inf;
+  * LSE is the natural log of the sum of exp over the visible *scaled* scores;
+  * GQA groups are contiguous: query head h reads K/V head h // (Hq // Hkv);
+  * decode attends to cache rows [0, seqlens[b]) with no mask (the caller has
+    already appended the new token's K/V).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Decode raw bf16 bit patterns exactly.
+
+    bf16 is the upper 16 bits of an IEEE-754 binary32 value, so shifting the
+    pattern into the high half of a 32-bit word and widening is exact.
+    """
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _kv_head(h: int, Hq: int, Hkv: int) -> int:
+    """Query head h shares the K/V head of its group ([PW] §2.3, MQA/GQA)."""
+    return h // (Hq // Hkv)
+
+
+def _two_pass_softmax(S: np.ndarray):
+    """Row softmax of a fully materialised score block ([MG-A] §2.4).
+
+    Pass 1 takes each row's max m and Z = sum_j exp(S_ij - m); pass 2 forms
+    P_ij = exp(S_ij - m) / Z. Subtracting the row max only changes the
+    representation, not the probabilities ([AUT] §8). Returns (P, lse) with
+    lse = m + ln Z. Rows whose scores are all -inf give P = 0, lse = -inf.
+    """
+    m = S.max(axis=1, initial=-np.inf)  # a row with no keys at all has max -inf
+    live = np.isfinite(m)
+    P = np.zeros_like(S)
+    Z = np.zeros_like(m)
+    E = np.exp(S[live] - m[live, None])  # masked entries: exp(-inf) = 0
+    Z[live] = E.sum(axis=1)
+    P[live] = E / Z[live, None]
+    lse = np.full(m.shape, -np.inf)
+    lse[live] = m[live] + np.log(Z[live])
+    return P, lse
+
+
+def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block: int = 1024):
+    """O = softmax(scale * Q K^T + mask) V per (batch, query head), and the LSE.
+
+    q: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (float64). Returns o [B, Hq, R, d]
+    and lse [B, Hq, R] where R = Nq, or len(rows) when a subset of query rows
+    is asked for (the definition is row-wise, so a subset is exact).
+
+    Steps ([MG-A] §2.2-§2.4, §4.1; [PW] §2.1): materialise
+    S_ij = scale * q_i . k_j for every visible pair; put -inf where the causal
+    rule hides key j from query i ([IMR], masking section); two-pass softmax
+    per row; O = P V. Rows are processed in blocks of ``row_block`` only to
+    bound memory: each row's full score vector is materialised before its
+    softmax, which is the same definition.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, dv = v.shape
+    assert k.shape == (B, Hkv, Nk, d) and Hq % Hkv == 0
+    rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    o = np.zeros((B, Hq, rows.size, dv))
+    lse = np.full((B, Hq, rows.size), -np.inf)
+    keys = np.arange(Nk)
+    for b in range(B):
+        for h in range(Hq):
+            kh = k[b, _kv_head(h, Hq, Hkv)]
+            vh = v[b, _kv_head(h, Hq, Hkv)]
+            for r0 in range(0, rows.size, row_block):
+                ri = rows[r0:r0 + row_block]
+                S = scale * (q[b, h, ri] @ kh.T)
+                if causal:
+                    hidden = keys[None, :] > (ri[:, None] + (Nk - Nq))
+                    S = np.where(hidden, -np.inf, S)
+                P, l = _two_pass_softmax(S)
+                o[b, h, r0:r0 + ri.size] = P @ vh
+                lse[b, h, r0:r0 + ri.size] = l
+    return o, lse
+
+
+def attention_decode(q, k_cache, v_cache, seqlens, scale: float):
+    """One decode step: each sequence's new query attends to its cached keys.
+
+    q: [B, Hq, d]; k_cache, v_cache: [B, Hkv, Lmax, d]; seqlens: [B] ints in
+    [0, Lmax]. The new token's query reads the cached K/V of positions
+    0..seqlens[b]-1 ([IMR], prefill/decode section; [PW] §3.1), with GQA head
+    sharing ([PW] §3.2). Returns o [B, Hq, d] and lse [B, Hq]; a sequence of
+    length 0 gives o = 0 and lse = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, d = q.shape
+    _, Hkv, Lmax, dv = v_cache.shape
+    o = np.zeros((B, Hq, dv))
+    lse = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        L = int(seqlens[b])
+        if not 0 <= L <= Lmax:
+            raise ValueError(f"seqlens[{b}]={L} outside [0, {Lmax}]")
+        for h in range(Hq):
+            kvh = _kv_head(h, Hq, Hkv)
+            S = scale * (q[b, h][None, :] @ np.asarray(k_cache[b, kvh, :L], np.float64).T)
+            P, l = _two_pass_softmax(S)
+            o[b, h] = (P @ np.asarray(v_cache[b, kvh, :L], np.float64))[0]
+            lse[b, h] = l[0]
+    return o, lse
+
+
+def online_attention_rows(q, k, v, scale: float, tile: int, causal_offset=None):
+    """The blockwise recurrence of [AUT] §8 (its first two equations), literally.
+
+    q: [n, d]; k, v: [Nk, d]. Keys are visited in tiles of ``tile``. Per query
+    row the state is the running max m, the denominator l and the
+    un-normalised weighted sum u. For each tile with scores s_j:
+        m' = max(m, max_j s_j)
+        l' = exp(m - m') l + sum_j exp(s_j - m')
+        u' = exp(m - m') u + sum_j exp(s_j - m') v_j
+    and finally o = u / l, lse = m + ln l. ``causal_offset`` (if given) hides
+    key j from query i when j > i + causal_offset. Starting state m = -inf,
+    l = 0, u = 0; a tile in which nothing is visible yet leaves the state
+    unchanged (exp(-inf - -inf) is never formed). Pure Python loops: meant
+    only for the tiny brute-force equivalence tests.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, Nk = q.shape[0], k.shape[0]
+    o = np.zeros((n, v.shape[1]))
+    lse = np.full(n, -np.inf)
+    for i in range(n):
+        m, l, u = -np.inf, 0.0, np.zeros(v.shape[1])
+        for t0 in range(0, Nk, tile):
+            js = range(t0, min(t0 + tile, Nk))
+            s = [(-np.inf if causal_offset is not None and j > i + causal_offset
+                  else scale * float(q[i] @ k[j])) for j in js]
+            m_new = max([m] + s)
+            if m_new == -np.inf:
+                continue
+            corr = np.exp(m - m_new)
+            p = [np.exp(sj - m_new) for sj in s]
+            l = corr * l + sum(p)
+            u = corr * u + sum(pj * v[j] for pj, j in zip(p, js))
+            m = m_new
+        if l > 0:
+            o[i] = u / l
+            lse[i] = m + np.log(l)
+    return o, lse
+
+
+def merge_two_blocks(m1, l1, o1, m2, l2, o2):
+    """Combine the softmax statistics of two key blocks ([MG-A] §6.3 steps 2-4).
+
+    Each block carries its row max m, its local exp-sum l (relative to m) and
+    its block-normalised output o. With m_new = max(m1, m2):
+        l_new = l1 exp(m1 - m_new) + l2 exp(m2 - m_new)
+        o_new = (l1 o1 exp(m1 - m_new) + l2 o2 exp(m2 - m_new)) / l_new
+    A block that saw no key (m = -inf, l = 0) contributes nothing. Works on
+    scalars or on aligned arrays of rows (o has one more trailing axis).
+    """
+    m1, l1, m2, l2 = (np.asarray(x, np.float64) for x in (m1, l1, m2, l2))
+    o1, o2 = np.asarray(o1, np.float64), np.asarray(o2, np.float64)
+    m_new = np.maximum(m1, m2)
+    live = np.isfinite(m_new)
+    safe = np.where(live, m_new, 0.0)
+    a1 = np.where(np.isfinite(m1), np.exp(np.where(np.isfinite(m1), m1, 0.0) - safe), 0.0) * l1
+    a2 = np.where(np.isfinite(m2), np.exp(np.where(np.isfinite(m2), m2, 0.0) - safe), 0.0) * l2
+    l_new = a1 + a2
+    denom = np.where(l_new > 0, l_new, 1.0)
+    o_new = (a1[..., None] * o1 + a2[..., None] * o2) / denom[..., None]
+    return m_new, l_new, o_new
+
+
+def score_bytes(n: int, heads: int = 1, bytes_per_score: int = 4) -> int:
+    """Bytes of an explicitly stored score matrix: heads * n^2 * bytes ([AUT] §4, §6)."""
+    return heads * n * n * bytes_per_score
+
+
+def kv_cache_bytes(layers: int, n: int, h_kv: int, d_h: int, bytes_per_scalar: int) -> int:
+    """KV cache size 2 * L * n * h_kv * d_h * b ([AUT] §9, third equation; [PW] §3.2)."""
+    return 2 * layers * n * h_kv * d_h * bytes_per_scalar

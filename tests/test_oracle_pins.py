@@ -1,0 +1,372 @@
+"""Pins for the fp64 oracle: facts that do not come from the oracle itself.
+
+Each test would fail under a plausible slip in the oracle (a dropped scale, a
+flipped sign, a wrong GQA index, a transposed operand, a wrong causal offset,
+a missing rescale in the recurrence). Sources are cited by page title and
+section; the key [MG-A], [MG-B], [AUT], [IMR], [PW] is spelled out in
+``oracle/__init__.py``.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import (
+    attention_decode,
+    attention_forward,
+    bf16_bits_to_f64,
+    kv_cache_bytes,
+    merge_two_blocks,
+    online_attention_rows,
+    score_bytes,
+)
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _rand(rng, *shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# --- worked examples (golden fixtures) -------------------------------------------------
+
+def test_two_key_worked_example(golden_dir):
+    """[MG-A] §2.4: weights exp(S_ij)/sum exp(S_ik); hand-worked 3/4, 1/4 split."""
+    g = _load(golden_dir, "two_key_softmax.json")
+    q = np.array(g["q"])[None, None]
+    k = np.array(g["k"])[None, None]
+    v = np.array(g["v"])[None, None]
+    o, lse = attention_forward(q, k, v, g["scale"], causal=False)
+    np.testing.assert_allclose(o[0, 0], g["o"], atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], g["lse"], atol=1e-12)
+
+
+def test_causal_three_token_worked_example(golden_dir):
+    """[IMR] masking: token t sees positions <= t; hand-worked weights 1, 1:2, 1:2:3."""
+    g = _load(golden_dir, "causal_three_tokens.json")
+    q = np.array(g["q"])[None, None]
+    k = np.array(g["k"])[None, None]
+    v = np.array(g["v"])[None, None]
+    o, lse = attention_forward(q, k, v, g["scale"], causal=True)
+    np.testing.assert_allclose(o[0, 0], g["o"], atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], g["lse"], atol=1e-12)
+    # the online recurrence must give the same numbers at every tiling
+    for tile in (1, 2, 3):
+        o2, l2 = online_attention_rows(np.array(g["q"]), np.array(g["k"]), np.array(g["v"]),
+                                       g["scale"], tile, causal_offset=0)
+        np.testing.assert_allclose(o2, g["o"], atol=1e-12)
+        np.testing.assert_allclose(l2, g["lse"], atol=1e-12)
+
+
+def test_score_matrix_bytes_match_pages(golden_dir):
+    """[AUT] §6: 1/4/16/64 MiB at N = 512..4096; [PW] §2.1: 32 heads at 4096 ~ 2 GB."""
+    g = _load(golden_dir, "score_bytes.json")
+    for n, mib in g["per_head_fp32_mib"].items():
+        assert score_bytes(int(n)) == mib * 2**20
+    assert score_bytes(4096, heads=32) == g["n4096_heads32_fp32_gib"] * 2**30
+    # quadratic growth: doubling n quadruples the bytes ([AUT] §4)
+    assert score_bytes(2048) == 4 * score_bytes(1024)
+
+
+def test_kv_cache_bytes_match_pages(golden_dir):
+    """[PW] §3.2 / §7.3 LLaMA-7B cache sizes from [AUT] §9 M_KV = 2 L n h_kv d_h b."""
+    g = _load(golden_dir, "kv_cache_bytes.json")
+    for c in g["cases"]:
+        got = kv_cache_bytes(c["layers"], c["n"], c["h_kv"], c["d_h"], c["b"])
+        want = c["mib"] * 2**20 if "mib" in c else c["gib"] * 2**30
+        assert got == want
+    assert 16 * kv_cache_bytes(32, 2048, 32, 128, 2) == g["batch16_n2048_layers32_gib"] * 2**30
+    r = g["gqa_ratio"]
+    assert kv_cache_bytes(1, 1, r["h_q"], 128, 2) == r["shrink"] * kv_cache_bytes(1, 1, r["h_kv"], 128, 2)
+
+
+# --- closed forms and invariants ----------------------------------------------------------
+
+def test_bf16_decoding_exact():
+    """bf16 is the top half of binary32: check named patterns and all 65536 against torch."""
+    named = {0x3F80: 1.0, 0xC000: -2.0, 0x3FC0: 1.5, 0x0000: 0.0, 0x7F80: np.inf,
+             0xFF80: -np.inf, 0x0001: 2.0**-133, 0x4049: 3.140625}
+    for bits, val in named.items():
+        assert bf16_bits_to_f64(np.array([bits], np.uint16))[0] == val
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = bf16_bits_to_f64(allbits)
+    ref = torch.from_numpy(allbits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    same = (ours == ref) | (np.isnan(ours) & np.isnan(ref))
+    assert same.all()
+
+
+def test_rows_are_probability_distributions():
+    """[MG-A] §2.4: each row of weights sums to 1; with V = I the output IS the weight row,
+    and weight ratios follow exp of score differences."""
+    rng = np.random.default_rng(1)
+    n, d = 9, 5
+    q, k = _rand(rng, 1, 1, n, d), _rand(rng, 1, 1, n, d)
+    scale = 0.37
+    P, _ = attention_forward(q, k, np.eye(n)[None, None], scale, causal=False)
+    P = P[0, 0]
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+    assert (P > 0).all()
+    s = scale * q[0, 0] @ k[0, 0].T
+    np.testing.assert_allclose(np.log(P[:, 1:] / P[:, :1]), s[:, 1:] - s[:, :1], atol=1e-10)
+    # causal: weights above the diagonal are exactly 0, rows still sum to 1
+    Pc, _ = attention_forward(q, k, np.eye(n)[None, None], scale, causal=True)
+    assert (np.triu(Pc[0, 0], 1) == 0).all()
+    np.testing.assert_allclose(Pc[0, 0].sum(axis=1), 1.0, atol=1e-12)
+
+
+def test_identical_keys_give_mean_of_values():
+    """All keys equal => uniform weights => O = mean(V), LSE = s + ln Nk ([MG-A] §2.4)."""
+    rng = np.random.default_rng(2)
+    Nk, d = 37, 8
+    q = _rand(rng, 1, 1, 5, d)
+    k = np.repeat(_rand(rng, 1, 1, 1, d), Nk, axis=2)
+    v = _rand(rng, 1, 1, Nk, d)
+    scale = 0.25
+    o, lse = attention_forward(q, k, v, scale, causal=False)
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0].mean(axis=0), (5, d)), atol=1e-12)
+    s = scale * (q[0, 0] @ k[0, 0, 0])
+    np.testing.assert_allclose(lse[0, 0], s + math.log(Nk), atol=1e-12)
+
+
+def test_causal_row_zero_is_first_value():
+    """[IMR] masking: row 0 sees only key 0 => O_0 = v_0 exactly, LSE_0 = scale q_0.k_0."""
+    rng = np.random.default_rng(3)
+    q, k, v = (_rand(rng, 2, 3, 16, 8) for _ in range(3))
+    o, lse = attention_forward(q, k, v, 0.5, causal=True)
+    assert np.array_equal(o[:, :, 0], v[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], 0.5 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0]),
+                               atol=1e-12)
+
+
+def test_single_key_returns_its_value():
+    rng = np.random.default_rng(4)
+    q, k, v = _rand(rng, 1, 2, 6, 4), _rand(rng, 1, 2, 1, 4), _rand(rng, 1, 2, 1, 4)
+    o, _ = attention_forward(q, k, v, 1.0, causal=False)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), atol=1e-15)
+
+
+def test_affine_in_values():
+    """O is a convex combination of value rows ([MG-A] §2.4), hence affine in V."""
+    rng = np.random.default_rng(5)
+    q, k, v = (_rand(rng, 1, 2, 11, 6) for _ in range(3))
+    for causal in (False, True):
+        o, _ = attention_forward(q, k, v, 0.4, causal)
+        o2, _ = attention_forward(q, k, 3.0 * v - 2.0, 0.4, causal)
+        np.testing.assert_allclose(o2, 3.0 * o - 2.0, atol=1e-12)
+
+
+def test_permutation_invariance_non_causal():
+    """Permuting (K, V) rows together changes nothing; permuting Q rows permutes O."""
+    rng = np.random.default_rng(6)
+    q, k, v = _rand(rng, 1, 1, 10, 5), _rand(rng, 1, 1, 13, 5), _rand(rng, 1, 1, 13, 3)
+    o, lse = attention_forward(q, k, v, 0.7, causal=False)
+    pk = rng.permutation(13)
+    o2, lse2 = attention_forward(q, k[:, :, pk], v[:, :, pk], 0.7, causal=False)
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, atol=1e-12)
+    pq = rng.permutation(10)
+    o3, _ = attention_forward(q[:, :, pq], k, v, 0.7, causal=False)
+    np.testing.assert_allclose(o3, o[:, :, pq], atol=1e-12)
+
+
+def test_large_scale_selects_best_matching_key():
+    """As the scale grows, softmax concentrates on the largest score: O -> v_argmax.
+    (A sign slip would select the smallest score instead.)"""
+    rng = np.random.default_rng(7)
+    q, k, v = _rand(rng, 1, 1, 6, 4), _rand(rng, 1, 1, 9, 4), _rand(rng, 1, 1, 9, 3)
+    s = q[0, 0] @ k[0, 0].T
+    o, _ = attention_forward(q, k, v, 1e4, causal=False)
+    np.testing.assert_allclose(o[0, 0], v[0, 0][s.argmax(axis=1)], atol=1e-9)
+
+
+def test_cross_attention_bottom_right_causal_alignment():
+    """Nq != Nk causal: the last query sees every key, query i sees keys j <= i + Nk - Nq;
+    the no-key rows (Nq > Nk) give O = 0, LSE = -inf."""
+    rng = np.random.default_rng(8)
+    q, k, v = _rand(rng, 1, 1, 4, 3), _rand(rng, 1, 1, 7, 3), _rand(rng, 1, 1, 7, 2)
+    o, lse = attention_forward(q, k, v, 1.0, causal=True)
+    full, fl = attention_forward(q[:, :, 3:], k, v, 1.0, causal=False)
+    np.testing.assert_allclose(o[:, :, 3:], full, atol=1e-12)
+    np.testing.assert_allclose(lse[:, :, 3:], fl, atol=1e-12)
+    first, f0 = attention_forward(q[:, :, :1], k[:, :, :4], v[:, :, :4], 1.0, causal=False)
+    np.testing.assert_allclose(o[:, :, :1], first, atol=1e-12)
+    q2 = _rand(rng, 1, 1, 6, 3)
+    o2, l2 = attention_forward(q2, k[:, :, :2], v[:, :, :2], 1.0, causal=True)
+    assert (o2[0, 0, :4] == 0).all() and np.isneginf(l2[0, 0, :4]).all()
+    np.testing.assert_allclose(o2[0, 0, 5], attention_forward(q2[:, :, 5:], k[:, :, :2], v[:, :, :2],
+                                                              1.0, False)[0][0, 0, 0], atol=1e-12)
+
+
+# --- independent library routine ----------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dv,causal", [
+    (2, 4, 4, 33, 33, 16, 16, False),
+    (1, 6, 2, 40, 40, 8, 8, True),       # GQA: contiguous groups of 3
+    (1, 4, 1, 17, 29, 8, 12, False),     # MQA, rectangular, d != dv
+    (2, 8, 2, 21, 50, 16, 16, True),     # GQA, causal rectangular (bottom-right)
+])
+def test_matches_torch_sdpa_fp64(B, Hq, Hkv, Nq, Nk, d, dv, causal):
+    """torch's scaled_dot_product_attention (CPU, fp64) is an independent implementation."""
+    rng = np.random.default_rng(9 + Nq)
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, dv)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = attention_forward(q, k, v, scale, causal)
+    tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+    g = Hq // Hkv
+    tk, tv = tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1)
+    mask = None
+    if causal:
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = j <= i + (Nk - Nq)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+    s = torch.einsum("bhid,bhjd->bhij", tq, tk) * scale
+    if mask is not None:
+        s = s.masked_fill(~mask, -math.inf)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+def test_row_subset_is_exact():
+    rng = np.random.default_rng(10)
+    q, k, v = _rand(rng, 1, 2, 50, 8), _rand(rng, 1, 1, 50, 8), _rand(rng, 1, 1, 50, 8)
+    o, lse = attention_forward(q, k, v, 0.3, True, row_block=7)
+    rows = np.array([0, 3, 17, 49])
+    o2, lse2 = attention_forward(q, k, v, 0.3, True, rows=rows)
+    np.testing.assert_allclose(o2, o[:, :, rows], atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[:, :, rows], atol=1e-13)
+
+
+# --- the online recurrence equals the two-pass definition ([AUT] §8; [PW] §4.2) -----------
+
+def _adversarial_keys(rng, n, d, kind):
+    q = _rand(rng, 1, d)
+    base = _rand(rng, n, d)
+    if kind == "random":
+        return q, base
+    # scores that rise (new max every tile) or fall (max fixed by the first key)
+    direction = q[0] / np.linalg.norm(q[0])
+    ramp = np.linspace(-6, 6, n) if kind == "rising" else np.linspace(6, -6, n)
+    return q, base * 0.1 + ramp[:, None] * direction[None, :] * 3
+
+
+@pytest.mark.parametrize("kind", ["random", "rising", "falling"])
+def test_online_recurrence_equals_two_pass_all_tilings(kind):
+    rng = np.random.default_rng(11)
+    for n_keys in (1, 2, 5, 16):
+        for d in (1, 3, 8):
+            q1, k = _adversarial_keys(rng, n_keys, d, kind)
+            q = np.concatenate([q1, _rand(rng, 3, d)])
+            v = _rand(rng, n_keys, d)
+            ref_o, ref_l = attention_forward(q[None, None], k[None, None], v[None, None], 0.9, False)
+            for tile in range(1, n_keys + 1):
+                o, lse = online_attention_rows(q, k, v, 0.9, tile)
+                np.testing.assert_allclose(o, ref_o[0, 0], atol=1e-12, rtol=1e-12)
+                np.testing.assert_allclose(lse, ref_l[0, 0], atol=1e-12, rtol=1e-12)
+
+
+def test_online_recurrence_causal_and_empty_rows():
+    rng = np.random.default_rng(12)
+    n, Nk, d = 6, 9, 4
+    q, k, v = _rand(rng, n, d), _rand(rng, Nk, d), _rand(rng, Nk, d)
+    for offset in (-3, 0, 3):   # Nk - Nq offsets; -3 leaves rows with no visible key
+        Nq = Nk - offset
+        qq = _rand(rng, Nq, d) if Nq != n else q
+        ref_o, ref_l = attention_forward(qq[None, None], k[None, None], v[None, None], 1.1, True)
+        for tile in range(1, Nk + 1):
+            o, lse = online_attention_rows(qq, k, v, 1.1, tile, causal_offset=offset)
+            np.testing.assert_allclose(o, ref_o[0, 0], atol=1e-12)
+            np.testing.assert_allclose(lse, ref_l[0, 0], atol=1e-12)
+
+
+def test_equivalence_check_catches_a_missing_rescale():
+    """Plant a mistake in a copy of the recurrence (drop the exp(m - m') factor on u):
+    the equivalence check above must then fail on keys whose max keeps rising."""
+    rng = np.random.default_rng(15)
+    q, k = _adversarial_keys(rng, 8, 4, "rising")
+    v = _rand(rng, 8, 4)
+
+    def broken(tile):
+        m, l, u = -np.inf, 0.0, np.zeros(4)
+        for t0 in range(0, 8, tile):
+            s = [float(q[0] @ k[j]) for j in range(t0, t0 + tile)]
+            m_new = max([m] + s)
+            corr = np.exp(m - m_new)
+            p = [np.exp(x - m_new) for x in s]
+            l = corr * l + sum(p)
+            u = u + sum(pj * v[t0 + i] for i, pj in enumerate(p))   # planted: no corr
+            m = m_new
+        return u / l
+
+    ref, _ = attention_forward(q[None, None], k[None, None], v[None, None], 1.0, False)
+    good, _ = online_attention_rows(q, k, v, 1.0, 2)
+    np.testing.assert_allclose(good[0], ref[0, 0, 0], atol=1e-12)
+    assert np.abs(broken(2) - ref[0, 0, 0]).max() > 1e-3
+
+
+def test_two_block_merge_equals_full_softmax():
+    """[MG-A] §6.3: merging (m, l, O) of two key blocks reproduces the full result,
+    at every split point, including a block that sees nothing."""
+    rng = np.random.default_rng(13)
+    Nq, Nk, d = 7, 12, 5
+    q, k, v = _rand(rng, Nq, d), _rand(rng, Nk, d), _rand(rng, Nk, d)
+    ref_o, ref_l = attention_forward(q[None, None], k[None, None], v[None, None], 0.8, False)
+    for cut in range(1, Nk):
+        stats = []
+        for sl in (slice(0, cut), slice(cut, Nk)):
+            o_b, lse_b = attention_forward(q[None, None], k[None, None, sl], v[None, None, sl], 0.8, False)
+            m_b = (0.8 * q @ k[sl].T).max(axis=1)
+            stats.append((m_b, np.exp(lse_b[0, 0] - m_b), o_b[0, 0]))
+        m, l, o = merge_two_blocks(*stats[0], *stats[1])
+        np.testing.assert_allclose(o, ref_o[0, 0], atol=1e-12)
+        np.testing.assert_allclose(m + np.log(l), ref_l[0, 0], atol=1e-12)
+    empty = (np.full(Nq, -np.inf), np.zeros(Nq), np.zeros((Nq, d)))
+    m_full = (0.8 * q @ k.T).max(axis=1)
+    full = (m_full, np.exp(ref_l[0, 0] - m_full), ref_o[0, 0])
+    for a, b in ((empty, full), (full, empty)):
+        m, l, o = merge_two_blocks(*a, *b)
+        np.testing.assert_allclose(o, ref_o[0, 0], atol=1e-12)
+    m, l, o = merge_two_blocks(*empty, *empty)
+    assert (l == 0).all() and (o == 0).all()
+
+
+# --- decode -------------------------------------------------------------------------------
+
+def test_decode_matches_prefix_attention_and_sdpa():
+    """Decode = one query over the cached prefix [0, L) ([IMR] prefill/decode; [PW] §3.1)."""
+    rng = np.random.default_rng(14)
+    B, Hq, Hkv, Lmax, d = 3, 8, 2, 40, 16
+    q, kc, vc = _rand(rng, B, Hq, d), _rand(rng, B, Hkv, Lmax, d), _rand(rng, B, Hkv, Lmax, d)
+    seqlens = np.array([1, 23, 40])
+    scale = 1 / math.sqrt(d)
+    o, lse = attention_decode(q, kc, vc, seqlens, scale)
+    for b in range(B):
+        L = seqlens[b]
+        tq = torch.from_numpy(q[b][:, None, :])
+        tk = torch.from_numpy(kc[b, :, :L]).repeat_interleave(Hq // Hkv, dim=0)
+        tv = torch.from_numpy(vc[b, :, :L]).repeat_interleave(Hq // Hkv, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+        np.testing.assert_allclose(o[b], ref[:, 0].numpy(), atol=1e-12)
+        s = torch.einsum("hd,hjd->hj", tq[:, 0], tk) * scale
+        np.testing.assert_allclose(lse[b], torch.logsumexp(s, -1).numpy(), atol=1e-12)
+    # the cache tail past seqlens is never read
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[0, :, 1:] = 1e30
+    vc2[1, :, 23:] = np.nan
+    o2, lse2 = attention_decode(q, kc2, vc2, seqlens, scale)
+    np.testing.assert_array_equal(o2, o)
+    np.testing.assert_array_equal(lse2, lse)
+    # length 1: the only cached value; length 0: zero output, -inf lse
+    np.testing.assert_allclose(o[0], vc[0].repeat(Hq // Hkv, axis=0)[:, 0], atol=1e-15)
+    o0, l0 = attention_decode(q, kc, vc, np.array([0, 0, 5]), scale)
+    assert (o0[:2] == 0).all() and np.isneginf(l0[:2]).all()
+    with pytest.raises(ValueError):
+        attention_decode(q, kc, vc, np.array([1, 41, 2]), scale)
