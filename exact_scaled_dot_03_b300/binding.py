@@ -1,0 +1,159 @@
+"""Thin Python binding over the C ABI in ``include/attn.h``.
+
+Argument marshalling only: PyTorch tensors supply device memory and the
+current CUDA stream; every step of the computation runs in the CUDA library.
+If the library has not been built, or a call fails, this raises instead of
+computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_NAME = "libattn_sm103.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_ARG = range(6)
+
+# name -> (restype, argtypes): the exported surface of include/attn.h
+_vp, _i, _f, _sz, _i64, _u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                                ctypes.c_int64, ctypes.c_uint64)
+SIGNATURES = {
+    "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_status_string": (ctypes.c_char_p, [_i]),
+    "attn_score_bytes": (_u64, [_i64, _i64, _i]),
+    "attn_kv_cache_bytes": (_u64, [_i64, _i64, _i64, _i64, _i]),
+    "attn_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code) if _lib is not None else code} (status {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_NAME} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().attn_status_string(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise AttnError(code, where)
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16, dims=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d) rounded to fp32 (the pages' score scaling)."""
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+        stream=None):
+    """Exact attention forward: returns (o, lse); see ``attn_fwd`` in include/attn.h.
+
+    q: [B, Hq, Nq, d], k/v: [B, Hkv, Nk, d], bf16 CUDA tensors.
+    """
+    _need(q, "q", dims=4)
+    _need(k, "k", dims=4)
+    _need(v, "v", dims=4)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if k.shape != v.shape or Bk != B or dk != d:
+        raise ValueError("q/k/v shapes disagree")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out", dims=4)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", dtype=torch.float32, dims=3)
+    s = default_scale(d) if scale is None else float(scale)
+    code = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr() if lse is not None else None,
+                          B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)), _stream_handle(stream))
+    _check(code, "attn_fwd")
+    return o, lse
+
+
+def decode_workspace_size(B: int, Hq: int, Hkv: int, Lmax: int, d: int) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, Hkv, Lmax, d))
+
+
+def decode_workspace(B: int, Hq: int, Hkv: int, Lmax: int, d: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (the library keeps it zeroed between calls)."""
+    n = decode_workspace_size(B, Hq, Hkv, Lmax, d)
+    if n == 0:
+        raise AttnError(ERR_UNSUPPORTED, "attn_decode_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode(q, k_cache, v_cache, seqlens, scale: float | None = None, workspace=None, out=None, lse=None,
+           want_lse: bool = True, stream=None):
+    """KV-cache decode: returns (o, lse); see ``attn_decode`` in include/attn.h.
+
+    q: [B, Hq, d]; caches: [B, Hkv, Lmax, d] bf16; seqlens: [B] int32 (all CUDA).
+    """
+    _need(q, "q", dims=3)
+    _need(k_cache, "k_cache", dims=4)
+    _need(v_cache, "v_cache", dims=4)
+    _need(seqlens, "seqlens", dtype=torch.int32, dims=1)
+    B, Hq, d = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, Lmax, d, device=q.device)
+    _need(workspace, "workspace", dtype=torch.uint8, dims=1)
+    o = torch.empty_like(q) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    s = default_scale(d) if scale is None else float(scale)
+    code = lib().attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(),
+                             o.data_ptr(), lse.data_ptr() if lse is not None else None,
+                             B, Hq, Hkv, Lmax, d, s, workspace.data_ptr(), workspace.numel(),
+                             _stream_handle(stream))
+    _check(code, "attn_decode")
+    return o, lse
+
+
+def device_status(stream=None):
+    """Synchronise the stream and read/clear the device status: (code, [flags, site, block])."""
+    detail = (ctypes.c_uint * 3)()
+    code = lib().attn_device_status(_stream_handle(stream), detail)
+    return code, list(detail)

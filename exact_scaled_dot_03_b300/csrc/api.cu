@@ -1,0 +1,300 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// TMA tensor-map encoding, launch configuration and the device status word.
+// Everything the caller asks for runs in the kernels of fwd_kernel.cuh and
+// decode_kernel.cuh; there is no host or library fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "decode_kernel.cuh"
+#include "fwd_kernel.cuh"
+
+namespace {
+
+using namespace attn_dev;
+
+// Per-device status word: {flags, wait site, block index, unused}.
+__device__ unsigned g_attn_status[4];
+
+constexpr int kMaxDevices = 64;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+unsigned* status_ptr(int dev) {
+  static unsigned* ptrs[kMaxDevices] = {};
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows_outer, n, d] bf16 tensor viewed as a 3-D TMA map with a
+// {64 columns, box_rows rows, 1} box and 128-byte swizzle. Rows past n read
+// as zeros.
+bool make_map(CUtensorMap* map, const void* base, int d, long long n, long long outer, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename K>
+bool ensure_smem(K kernel, int bytes, int dev, bool* done) {
+  if (done[dev]) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done[dev] = true;
+  return true;
+}
+
+// o = 0 and lse = -inf for rows that see no key at all.
+__global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, size_t rows, int d) {
+  const size_t n = rows * static_cast<size_t>(d);
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    o[i] = __float2bfloat16_rn(0.f);
+    if (lse != nullptr && i % d == 0) lse[i / d] = -CUDART_INF_F;
+  }
+}
+
+template <int D>
+attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, float scale, int causal, cudaStream_t stream, int dev) {
+  static bool smem_set[kMaxDevices] = {};
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, 128) ||
+      !make_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, 128) ||
+      !make_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, 128))
+    return ATTN_ERR_CUDA;
+  if (!ensure_smem(attn_fwd_kernel<D>, C::SMEM_BYTES, dev, smem_set)) return ATTN_ERR_CUDA;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.group = Hq / Hkv;
+  a.causal = causal;
+  a.causal_offset = Nk - Nq;
+  a.num_pairs = (Nq + 255) / 256;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.status = status_ptr(dev);
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  dim3 grid(Hq, a.num_pairs, B);
+  attn_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+struct DecodePlan {
+  int G, GC, qgroups, units, split, max_splits;
+  size_t part_o_off, part_lse_off, ticket_off, total;
+};
+
+bool plan_decode(int B, int Hq, int Hkv, int Lmax, int d, DecodePlan* p) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return false;
+  if (d != 64 && d != 128) return false;
+  p->G = Hq / Hkv;
+  p->GC = p->G % 8 == 0 ? 8 : p->G % 4 == 0 ? 4 : p->G % 2 == 0 ? 2 : 1;
+  p->qgroups = p->G / p->GC;
+  const long long units = static_cast<long long>(B) * Hkv * p->qgroups;
+  if (units > 65535) return false;
+  p->units = static_cast<int>(units);
+  p->split = 512;  // keys per CTA; a multiple of the 64-key tile
+  p->max_splits = (Lmax + p->split - 1) / p->split;
+  const size_t slots = static_cast<size_t>(p->units) * p->max_splits * p->GC;
+  p->part_o_off = 0;
+  p->part_lse_off = slots * d * sizeof(float);
+  p->ticket_off = p->part_lse_off + ((slots * sizeof(float) + 15) & ~size_t(15));
+  p->total = p->ticket_off + ((static_cast<size_t>(p->units) * sizeof(int) + 15) & ~size_t(15));
+  return true;
+}
+
+template <int D, int GC>
+attn_status launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seqlens, void* o,
+                          float* lse, int B, int Hq, int Hkv, int Lmax, float scale, void* ws,
+                          const DecodePlan& plan, cudaStream_t stream, int dev) {
+  static bool smem_set[kMaxDevices] = {};
+  using C = DecCfg<D, GC>;
+  CUtensorMap tk, tv;
+  if (!make_map(&tk, kc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK) ||
+      !make_map(&tv, vc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK))
+    return ATTN_ERR_CUDA;
+  if (!ensure_smem(attn_decode_kernel<D, GC>, C::SMEM_BYTES, dev, smem_set)) return ATTN_ERR_CUDA;
+  DecArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.seqlens = seqlens;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.part_o = reinterpret_cast<float*>(w + plan.part_o_off);
+  a.part_lse = reinterpret_cast<float*>(w + plan.part_lse_off);
+  a.tickets = reinterpret_cast<int*>(w + plan.ticket_off);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.group = plan.G;
+  a.qgroups = plan.qgroups;
+  a.split = plan.split;
+  a.max_splits = plan.max_splits;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.status = status_ptr(dev);
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  dim3 grid(plan.max_splits, plan.units);
+  attn_decode_kernel<D, GC><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+attn_status dispatch_decode_gc(const void* q, const void* kc, const void* vc, const int32_t* seqlens, void* o,
+                               float* lse, int B, int Hq, int Hkv, int Lmax, float scale, void* ws,
+                               const DecodePlan& plan, cudaStream_t stream, int dev) {
+  switch (plan.GC) {
+    case 8: return launch_decode<D, 8>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
+    case 4: return launch_decode<D, 4>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
+    case 2: return launch_decode<D, 2>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
+    default: return launch_decode<D, 1>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  // k and v may be NULL only when there are no keys (an empty tensor has no storage).
+  if (q == nullptr || o == nullptr || (Nk > 0 && (k == nullptr || v == nullptr))) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;  // (NULL is aligned)
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || (Nq + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (Nq == 0) return ATTN_OK;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Nk == 0) {
+    const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+    const int blocks = static_cast<int>(std::min<size_t>((rows * d + 255) / 256, 148 * 16));
+    fill_empty_kernel<<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(o), lse, rows, d);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  if (d == 64) return launch_fwd<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, s, dev);
+  return launch_fwd<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, s, dev);
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d) {
+  DecodePlan p;
+  return plan_decode(B, Hq, Hkv, Lmax, d, &p) ? p.total : 0;
+}
+
+attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Lmax, int d, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seqlens == nullptr || o == nullptr ||
+      workspace == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(workspace, 16) || !aligned(seqlens, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  if (!plan_decode(B, Hq, Hkv, Lmax, d, &plan)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < plan.total) return ATTN_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return dispatch_decode_gc<64>(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, workspace, plan,
+                                  s, dev);
+  return dispatch_decode_gc<128>(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, workspace, plan, s,
+                                 dev);
+}
+
+attn_status attn_device_status(void* stream, unsigned* detail) {
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned words[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(words, g_attn_status, sizeof(words)) != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(g_attn_status, zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (detail != nullptr) {
+    detail[0] = words[0];
+    detail[1] = words[1];
+    detail[2] = words[2];
+  }
+  if (words[0] & kStatusWaitTimeout) return ATTN_ERR_TIMEOUT;
+  if (words[0] & kStatusBadSeqlen) return ATTN_ERR_DEVICE_ARG;
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_DEVICE_ARG: return "device saw a sequence length outside [0, Lmax]";
+  }
+  return "unknown status";
+}
+
+uint64_t attn_score_bytes(int64_t n, int64_t heads, int bytes_per_score) {
+  if (n < 0 || heads < 0 || bytes_per_score < 0) return 0;
+  return static_cast<uint64_t>(heads) * static_cast<uint64_t>(n) * static_cast<uint64_t>(n) *
+         static_cast<uint64_t>(bytes_per_score);
+}
+
+uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_h, int bytes_per_scalar) {
+  if (layers < 0 || n < 0 || h_kv < 0 || d_h < 0 || bytes_per_scalar < 0) return 0;
+  return 2ull * static_cast<uint64_t>(layers) * static_cast<uint64_t>(n) * static_cast<uint64_t>(h_kv) *
+         static_cast<uint64_t>(d_h) * static_cast<uint64_t>(bytes_per_scalar);
+}
+
+const char* attn_version(void) { return "exact-attn-sm103 0.1"; }
+
+}  // extern "C"

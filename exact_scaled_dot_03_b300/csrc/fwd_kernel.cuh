@@ -1,0 +1,384 @@
+// Exact attention forward (prefill / cross-attention) for sm_103a.
+//
+// What it computes: O = softmax(scale * Q K^T + causal mask) V and the row
+// log-sum-exp, per (batch, query head), with GQA/MQA head sharing
+// ([MG-A] §2.2-§2.4, §4.1; [PW] §2.1, §2.3). How: the score matrix is formed
+// one 128x128 tile at a time in tensor memory and never leaves the SM; each
+// query row keeps the running statistics of the blockwise softmax recurrence
+// ([AUT] §8, its first two equations; [MG-A] §6.3): running max m, denominator
+// l and the un-normalised sum u (held in TMEM), with o = u / l at the end.
+//
+// Sources: [MG-A] menggq.pages.dev "Transformer 架构的数学与计算深度解析";
+// [AUT] auturnal.com "从注意力到 IO 感知执行" (v10); [PW] pwwt.cn news 6124947.
+//
+// CTA = two 128-row query tiles of one (batch, head) sharing every K/V tile.
+//   warps 0-3 : softmax for query tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7 : softmax for query tile 1
+//   warp  8   : TMA producer (Q once, then the K/V ring)
+//   warp  9   : TMEM allocator + tcgen05.mma issuer
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
+// the bf16 probabilities P_t are written over the first 64 columns of S_t and
+// fed to the P.V MMA straight from TMEM.
+//
+// Rescaling is lazy: the reference max m of a row only moves when the new
+// tile's max exceeds it by more than 8 (in base-2 units). l and u always share
+// the same reference, so o = u / l is unchanged in exact arithmetic; the
+// exponentials stay <= 2^8, far from fp32/bf16 overflow.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace attn_dev {
+
+struct FwdArgs {
+  __nv_bfloat16* o;   // [B, Hq, Nq, D]
+  float* lse;         // [B, Hq, Nq] natural-log LSE, or nullptr
+  int B, Hq, Hkv, Nq, Nk;
+  int group;          // Hq / Hkv
+  int causal;
+  int causal_offset;  // Nk - Nq: query i sees key j iff j <= i + causal_offset
+  int num_pairs;      // ceil(Nq / 256)
+  float scale_log2;   // scale * log2(e)
+  unsigned* status;   // library status word (see kStatus*)
+};
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int BM = 128;                 // query rows per tile
+  static constexpr int BN = 128;                 // keys per K/V tile
+  static constexpr int KBLK = D / 64;            // 64-column (128-byte) swizzle blocks per row
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int BLOCK_BYTES = 128 * 64 * 2;     // one 128-row x 64-col swizzle block
+  static constexpr int TILE_BYTES = KBLK * BLOCK_BYTES;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 7;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + tmem base/abort words + alignment slack
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = 256;
+};
+
+// Wait sites (recorded in status[1] when a bounded wait gives up).
+enum : unsigned {
+  kSiteQFull = 1, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePvDoneMma, kSitePFull,
+  kSiteSFull, kSitePvDoneRescale, kSitePvDoneEpi, kSiteDrain, kSiteLoadDrain
+};
+
+// Number of 128-key tiles a 128-row query tile starting at row r0 must visit.
+__device__ __forceinline__ int fwd_num_kv_tiles(const FwdArgs& a, int r0) {
+  if (r0 >= a.Nq) return 0;
+  const int r_last = min(r0 + 127, a.Nq - 1);
+  const long long end = a.causal ? min((long long)a.Nk, (long long)r_last + a.causal_offset + 1)
+                                 : (long long)a.Nk;
+  return end <= 0 ? 0 : (int)((end + 127) / 128);
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sK = smem + C::K_OFF;
+  uint8_t* sV = smem + C::V_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::STAGES;
+  uint64_t* v_full = k_empty + C::STAGES;
+  uint64_t* v_empty = v_full + C::STAGES;
+  uint64_t* s_full = v_empty + C::STAGES;  // [2]
+  uint64_t* p_full = s_full + 2;           // [2]
+  uint64_t* pv_done = p_full + 2;          // [2]
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int pair = a.num_pairs - 1 - blockIdx.y;  // heaviest (latest) causal rows first
+  const int b = blockIdx.z;
+  const int hkv = h / a.group;
+  const int q_base = pair * 256;
+  int n_kv[2];
+  n_kv[0] = fwd_num_kv_tiles(a, q_base);
+  n_kv[1] = fwd_num_kv_tiles(a, q_base + 128);
+  const int n_kv_max = max(n_kv[0], n_kv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_full + t, 128);
+      mbar_init(pv_done + t, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kv_max > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t qbytes = 0;
+      for (int t = 0; t < 2; ++t) qbytes += n_kv[t] > 0 ? C::TILE_BYTES : 0;
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (n_kv[t] == 0) continue;
+        for (int kb = 0; kb < C::KBLK; ++kb)
+          tma_load_3d(sQ + t * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q_base + 128 * t,
+                      b * a.Hq + h);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv_max; ++j) {
+        const int s = j % C::STAGES;
+        const int u = j / C::STAGES;
+        if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, a.status, kSiteKEmpty)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(k_full + s, C::TILE_BYTES);
+        for (int kb = 0; kb < C::KBLK; ++kb)
+          tma_load_3d(sK + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_k, k_full + s, kb * 64, j * 128,
+                      b * a.Hkv + hkv);
+        if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, a.status, kSiteVEmpty)) {
+          *abort_flag = 1;
+          issued = j + 1;  // K of tile j is in flight, V is not
+          break;
+        }
+        mbar_arrive_expect_tx(v_full + s, C::TILE_BYTES);
+        for (int kb = 0; kb < C::KBLK; ++kb)
+          tma_load_3d(sV + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_v, v_full + s, kb * 64, j * 128,
+                      b * a.Hkv + hkv);
+        issued = j + 1;
+        if (*abort_flag) break;
+      }
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA exits.
+        mbar_wait(q_full, 0, a.status, kSiteLoadDrain);
+        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+          const int s = j % C::STAGES;
+          mbar_wait(k_full + s, (j / C::STAGES) & 1, a.status, kSiteLoadDrain);
+          mbar_wait(v_full + s, (j / C::STAGES) & 1, a.status, kSiteLoadDrain);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv_max > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      bool ok = mbar_wait(q_full, 0, a.status, kSiteQFull);
+      for (int j = 0; ok && j < n_kv_max; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull))) break;
+        tc_fence_after_sync();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_kv[t]) continue;
+          // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
+          if (j > 0) {
+            if (!(ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneMma))) break;
+            tc_fence_after_sync();
+          }
+          const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
+          const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+            umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
+                    smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full + t);
+        }
+        if (!ok) break;
+        umma_commit(k_empty + s);
+        if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull))) break;
+        tc_fence_after_sync();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_kv[t]) continue;
+          if (!(ok = mbar_wait(p_full + t, j & 1, a.status, kSitePFull))) break;
+          tc_fence_after_sync();
+          const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            umma_ts(tmem + C::O_COL + D * t, tmem + 128 * t + kk * 8,
+                    smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done + t);
+        }
+        if (!ok) break;
+        umma_commit(v_empty + s);
+      }
+      if (!ok) *abort_flag = 1;
+      // Every MMA issued above has finished before TMEM is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.status, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = q_base + 128 * t + wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128 * t;
+    const uint32_t tO = tmem + lane_off + C::O_COL + D * t;
+    const int nk = n_kv[t];
+    const float sl2 = a.scale_log2;
+    // key j is visible to this row iff j <= vis_last
+    const int vis_last = a.causal ? min(a.Nk - 1, row + a.causal_offset) : a.Nk - 1;
+    const int tile_first_vis = a.causal ? min(a.Nk - 1, q_base + 128 * t + a.causal_offset) : a.Nk - 1;
+    float m_used = -CUDART_INF_F;  // reference max, base-2 scaled units
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!(ok = mbar_wait(s_full + t, j & 1, a.status, kSiteSFull))) break;
+      tc_fence_after_sync();
+      float sv[128];
+      {
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_reg_fence(sr[c]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(sr[c][i]);
+        }
+      }
+      const int key0 = j * 128;
+      if (key0 + 127 > tile_first_vis) {  // tile-uniform: diagonal or ragged tail
+        const int rel = vis_last - key0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) sv[c] = (c > rel) ? -CUDART_INF_F : sv[c];
+      }
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, sv[c]);
+        mx1 = fmaxf(mx1, sv[c + 1]);
+        mx2 = fmaxf(mx2, sv[c + 2]);
+        mx3 = fmaxf(mx3, sv[c + 3]);
+      }
+      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool need = m_new > m_used + 8.0f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_used - m_new);  // 0 when m_used is still -inf
+        m_used = m_new;
+        l *= alpha;
+      }
+      // p = 2^(s * scale * log2(e) - m), packed to bf16 pairs over the first
+      // 64 columns of S (the scores are dead once read into registers).
+      const float m_ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 64 * half + 2 * i;
+          const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_ref));
+          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_ref));
+          l0 += p0;
+          l1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * half, pk);
+      }
+      l += l0 + l1;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // Bring the accumulated u onto the new reference before P.V adds to it.
+        if (!(ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneRescale))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + 32 * c, orr);
+          tmem_wait_ld();
+          tmem_reg_fence(orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(tO + 32 * c, orr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(p_full + t);
+    }
+    if (!ok) *abort_flag = 1;
+    // ---------------------------------------------------------- epilogue
+    bool have_o = false;
+    if (ok && nk > 0) {
+      ok = mbar_wait(pv_done + t, (nk - 1) & 1, a.status, kSitePvDoneEpi);
+      tc_fence_after_sync();
+      have_o = ok;
+    }
+    const bool in_range = row < a.Nq;
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = a.o + ((size_t)(b * a.Hq + h) * a.Nq + (in_range ? row : 0)) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t orr[32];
+      if (have_o) {
+        tmem_ld32(tO + 32 * c, orr);
+        tmem_wait_ld();
+        tmem_reg_fence(orr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) orr[i] = 0u;
+      }
+      uint32_t packed[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+      if (in_range) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+    if (a.lse != nullptr && in_range) {
+      a.lse[(size_t)(b * a.Hq + h) * a.Nq + row] =
+          l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace attn_dev

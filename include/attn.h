@@ -1,0 +1,144 @@
+/*
+ * exact attention for sm_103a (B300): C ABI.
+ *
+ * Computes exact multi-head scaled-dot-product attention
+ *     O = softmax(scale * Q K^T + causal mask) V
+ * tile by tile with the blockwise (online) softmax recurrence, so the score
+ * matrix never reaches device memory, plus the KV-cache decode form, with
+ * MHA / GQA / MQA head sharing. Sources, cited by page title and section:
+ *
+ *   [MG-A] menggq.pages.dev, "Transformer 架构的数学与计算深度解析：注意力机制的
+ *          详尽研究报告": §2.2 scores, §2.3 scaling, §2.4 softmax and weighted
+ *          sum, §4.1 causal mask, §4.2 cross-attention, §6.3 online softmax.
+ *   [AUT]  auturnal.com, "从注意力到 IO 感知执行：Transformer 的计算结构、复杂度
+ *          与可复核分析" (v10): §4/§6 score bytes, §8 (m, l, u recurrence,
+ *          first two equations), §9 (KV cache size, third equation).
+ *   [IMR]  imreese.github.io, "Transformer 笔记：注意力机制为什么会变成系统问题":
+ *          masking section, prefill/decode section.
+ *   [PW]   pwwt.cn news 6124947: §2.1 S = QK^T / sqrt(d_k), §2.3 MQA/GQA,
+ *          §3.1-3.2 KV cache, §4.2 tiling + online softmax is exact.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are bf16 (IEEE bfloat16 bit patterns), contiguous, row-major.
+ *     Device pointers must be 16-byte aligned (LSE pointers 4-byte aligned).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is asynchronous on that stream; no entry point
+ *     synchronises except attn_device_status().
+ *   - The caller owns every buffer, including the decode workspace. Nothing
+ *     here allocates or frees device memory.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is launched. Launch failures return ATTN_ERR_CUDA. Problems only the
+ *     device can see (a bounded internal wait that gave up, a sequence length
+ *     outside [0, Lmax]) are OR-ed into a per-device status word that
+ *     attn_device_status() reads and clears.
+ *   - GQA mapping: Hq % Hkv == 0 and query head h reads K/V head
+ *     h / (Hq / Hkv) (contiguous groups; [PW] §2.3). Hkv == Hq is MHA,
+ *     Hkv == 1 is MQA.
+ *   - Head dimension d (= d_k = d_v) must be 64 or 128; anything else returns
+ *     ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef EXACT_ATTN_SM103_H
+#define EXACT_ATTN_SM103_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128}) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  ATTN_ERR_TIMEOUT = 4,     /* (device) an internal pipeline wait gave up */
+  ATTN_ERR_DEVICE_ARG = 5   /* (device) a decode sequence length was outside [0, Lmax] */
+} attn_status;
+
+/*
+ * Prefill / cross-attention forward ([MG-A] §2.2-§2.4, §4.1-§4.2, §6.3;
+ * [AUT] §8; [PW] §2.1, §4.2).
+ *
+ *   q   [B, Hq,  Nq, d] bf16 (device)    k, v [B, Hkv, Nk, d] bf16 (device)
+ *   o   [B, Hq,  Nq, d] bf16 (device, written)
+ *   lse [B, Hq,  Nq] fp32 (device, written) or NULL: natural log of the sum of
+ *       exp(scale * q_i . k_j) over the keys row i sees; -inf for a row that
+ *       sees no key (its o row is 0).
+ *   scale: multiplies every score before the mask; must be finite and > 0
+ *       (1/sqrt(d) gives the pages' scaled dot product, [MG-A] §2.3).
+ *   causal: 0 = every query sees every key. 1 = query i sees key j iff
+ *       j <= i + (Nk - Nq), i.e. the last query is aligned with the last key;
+ *       for Nq == Nk this is the pages' rule j <= i ([IMR] masking section).
+ *   Sizes: B, Hq, Hkv >= 1; Nq, Nk >= 0 (Nq == 0 is a no-op; Nk == 0 gives
+ *       o = 0, lse = -inf, and k / v may then be NULL); ceil(Nq / 256) <=
+ *       65535; B <= 65535.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, void* stream);
+
+/*
+ * Size in bytes of the device workspace attn_decode needs for these sizes
+ * (split-KV partial results and one ticket per (sequence, KV head, query
+ * group)). Returns 0 for arguments attn_decode would reject. The workspace
+ * must be zero-filled before its first use; every call that completes
+ * leaves it zero-filled again, so it can be reused across calls on one
+ * stream (calls that overlap on the device must use separate workspaces).
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d);
+
+/*
+ * KV-cache decode: one new query token per sequence attends to its cached
+ * keys/values 0 .. seqlens[b]-1 ([IMR] prefill/decode section; [PW] §3.1-§3.2).
+ * The caller has already appended the new token's K/V to the cache.
+ *
+ *   q        [B, Hq, d] bf16 (device)
+ *   k_cache, v_cache [B, Hkv, Lmax, d] bf16 (device); rows at or past
+ *            seqlens[b] are never used in the result.
+ *   seqlens  [B] int32 (device), each in [0, Lmax]. A length of 0 gives
+ *            o = 0, lse = -inf. A value outside the range is clamped into it
+ *            and flagged in the device status (ATTN_ERR_DEVICE_ARG).
+ *   o        [B, Hq, d] bf16 (device, written)
+ *   lse      [B, Hq] fp32 (device, written) or NULL (natural log, as attn_fwd)
+ *   workspace / workspace_bytes: device buffer of at least
+ *            attn_decode_workspace_size(B, Hq, Hkv, Lmax, d) bytes, 16-byte
+ *            aligned, zero-filled before first use (see above).
+ */
+ATTN_API attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Lmax, int d, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling thread's current
+ * device's status word. Returns ATTN_OK, ATTN_ERR_TIMEOUT or
+ * ATTN_ERR_DEVICE_ARG (timeout wins if both are set), or ATTN_ERR_CUDA if
+ * the synchronisation itself failed. If `detail` is not NULL it receives the
+ * raw words {flags, wait site, block index}.
+ */
+ATTN_API attn_status attn_device_status(void* stream, unsigned* detail);
+
+/* Human-readable name of a status code (static string, never NULL). */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/* Bytes of an explicitly stored score matrix: heads * n^2 * bytes_per_score
+ * ([AUT] §4 and §6: 512/1024/2048/4096 -> 1/4/16/64 MiB per fp32 head). */
+ATTN_API uint64_t attn_score_bytes(int64_t n, int64_t heads, int bytes_per_score);
+
+/* KV cache bytes 2 * layers * n * h_kv * d_h * bytes ([AUT] §9, third
+ * equation; [PW] §3.2). */
+ATTN_API uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_h, int bytes_per_scalar);
+
+/* Library version string, e.g. "exact-attn-sm103 0.1". */
+ATTN_API const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTN_SM103_H */

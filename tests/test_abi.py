@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every symbol include/attn.h declares, and
+rejects bad arguments on the host before anything is launched. No GPU needed:
+only host-side entry points and argument checks run here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_scaled_dot_03_b300 import binding
+from exact_scaled_dot_03_b300 import build as buildmod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    buildmod.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 8
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(binding.SIGNATURES), "binding and header disagree"
+
+
+def test_host_helpers(lib):
+    assert lib.attn_version().startswith(b"exact-attn-sm103")
+    for code in range(6):
+        assert len(binding.status_string(code)) > 0
+    # score bytes ([AUT] §6) and KV cache bytes ([PW] §3.2) through the C ABI
+    assert [lib.attn_score_bytes(n, 1, 4) for n in (512, 1024, 2048, 4096)] == [m * 2**20 for m in (1, 4, 16, 64)]
+    assert lib.attn_score_bytes(4096, 32, 4) == 2 * 2**30
+    assert lib.attn_kv_cache_bytes(1, 2048, 32, 128, 2) == 32 * 2**20
+    assert lib.attn_kv_cache_bytes(32, 8192, 32, 128, 2) == 4 * 2**30
+    assert lib.attn_kv_cache_bytes(-1, 1, 1, 1, 1) == 0
+
+
+def test_decode_workspace_size(lib):
+    ws = binding.decode_workspace_size(16, 32, 8, 8192, 128)
+    # 128 units x 16 splits x 4 heads x (128 values + 1 lse) fp32 + tickets
+    assert ws >= 128 * 16 * 4 * 129 * 4
+    assert binding.decode_workspace_size(16, 32, 8, 8192, 96) == 0     # unsupported d
+    assert binding.decode_workspace_size(16, 30, 8, 8192, 128) == 0    # Hq % Hkv != 0
+    assert binding.decode_workspace_size(0, 32, 8, 8192, 128) == 0
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address: never dereferenced on these paths
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=16, Nk=16, d=64, scale=0.125,
+         causal=0):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ERR_INVALID_ARG),
+    (dict(o=None), binding.ERR_INVALID_ARG),
+    (dict(k=None), binding.ERR_INVALID_ARG),
+    (dict(v=None, Nq=0), binding.ERR_INVALID_ARG),
+    (dict(B=0), binding.ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), binding.ERR_INVALID_ARG),
+    (dict(Nq=-1), binding.ERR_INVALID_ARG),
+    (dict(causal=2), binding.ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.ERR_INVALID_ARG),
+    (dict(scale=-1.0), binding.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), binding.ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), binding.ERR_INVALID_ARG),
+    (dict(d=96), binding.ERR_UNSUPPORTED),
+    (dict(d=256), binding.ERR_UNSUPPORTED),
+    (dict(B=70000), binding.ERR_UNSUPPORTED),
+    (dict(Nq=0), binding.OK),   # empty: nothing to do, nothing launched
+])
+def test_fwd_argument_checks(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _dec(lib, q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Lmax=100, d=128,
+         scale=0.1, ws=FAKE, wsb=1 << 30):
+    return lib.attn_decode(q, kc, vc, sl, o, lse, B, Hq, Hkv, Lmax, d, scale, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sl=None), binding.ERR_INVALID_ARG),
+    (dict(ws=None), binding.ERR_INVALID_ARG),
+    (dict(wsb=16), binding.ERR_INVALID_ARG),
+    (dict(Lmax=0), binding.ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), binding.ERR_INVALID_ARG),
+    (dict(sl=FAKE + 2), binding.ERR_INVALID_ARG),
+    (dict(kc=FAKE + 4), binding.ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.ERR_INVALID_ARG),
+    (dict(d=80), binding.ERR_UNSUPPORTED),
+    (dict(B=40000, Hkv=2), binding.ERR_UNSUPPORTED),  # too many (sequence, head) units for one grid
+])
+def test_decode_argument_checks(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+def test_product_path_has_no_fallback(monkeypatch, tmp_path):
+    """Without the built library the binding raises; it never computes another way."""
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()
