@@ -1,0 +1,421 @@
+"""Benchmark: exact causal attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--prefill NAME] [--no-cpu-baseline] [--no-e2e]
+
+One step = one pass of the whole hot path over synthetic bf16 inputs that are
+already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
+N=16384, d=128) followed by a decode step (B=16, Hq=32, Hkv=8, d=128, cache
+lengths uniform on [1024, 8192]). L2 is flushed (a 256 MiB write) before each
+of the two launches, outside their CUDA-event brackets. Prints one JSON line.
+
+``value`` is prefill TFLOP/s (4*B*Hq*Nq*Nk*d, halved for causal) over the
+prefill launches; the decode result sits in ``decode`` (GB/s of the cache
+rows actually read, sum(seqlens)*Hkv*d*2*2 bytes, plus q, o and lse).
+Under torchrun every rank runs the same workload (replicas; weak scaling)
+and rank 0 prints the aggregate over the max-over-ranks time.
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
+of the same workload per step, on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_scaled_dot_03_b300 import workloads as W  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (bf16, causal) and decode GB/s; % of B300 roofline"
+PREFILL = {w.name: w for w in W.PREFILL_WORKLOADS}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "exact_scaled_dot_03_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_name, files):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_sha", "dram_bytes_per_launch")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_sha") != kernel_source_hash(files):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_prefill_sample(w, q, k, v, h, r0, r1):
+    """Time the oracle on query rows [r0, r1) of head h; return (useful flops, seconds)."""
+    import oracle
+    from exact_scaled_dot_03_b300.workloads import bf16_bits
+    hk = h // (w.Hq // w.Hkv)
+    qd = oracle.bf16_bits_to_f64(bf16_bits(q[:1, h:h + 1]))
+    kd = oracle.bf16_bits_to_f64(bf16_bits(k[:1, hk:hk + 1]))
+    vd = oracle.bf16_bits_to_f64(bf16_bits(v[:1, hk:hk + 1]))
+    rows = np.arange(r0, r1)
+    t0 = time.perf_counter()
+    oracle.attention_forward(qd, kd, vd, w.scale, w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    visible = (np.minimum(rows + (w.Nk - w.Nq), w.Nk - 1) + 1).clip(0).sum() if w.causal else rows.size * w.Nk
+    return 4.0 * w.d * float(visible), dt
+
+
+def oracle_decode_sample(w, q, kc, vc, sl, bs):
+    import oracle
+    from exact_scaled_dot_03_b300.workloads import bf16_bits
+    sel = list(bs)
+    qd = oracle.bf16_bits_to_f64(bf16_bits(q[sel]))
+    kd = oracle.bf16_bits_to_f64(bf16_bits(kc[sel]))
+    vd = oracle.bf16_bits_to_f64(bf16_bits(vc[sel]))
+    t0 = time.perf_counter()
+    oracle.attention_decode(qd, kd, vd, sl[sel].numpy(), w.scale)
+    dt = time.perf_counter() - t0
+    nbytes = int(sl[sel].sum()) * w.Hkv * w.d * 2 * 2
+    return nbytes, dt
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, q, k, v, budget_s=12.0):
+    """The oracle on a bounded sample: 512-row blocks from the last (heaviest)
+    rows of successive heads until the time budget is used."""
+    flops, secs, blocks = 0.0, 0.0, []
+    h, r1 = 0, w.Nq
+    while secs < budget_s and len(blocks) < 64:
+        r0 = max(0, r1 - 512)
+        f, dt = oracle_prefill_sample(w, q, k, v, h, r0, r1)
+        flops += f
+        secs += dt
+        blocks.append((h, r0, r1))
+        h = (h + 1) % w.Hq
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{len(blocks)} blocks of 512 query rows (the last rows, heaviest under the causal mask) "
+                      f"of heads 0..{len(blocks) - 1} of {w.name}; {secs:.1f} s of fp64 numpy on the host"}
+
+
+def run_reference(args, w, wd):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v = W.prefill_inputs(w)
+    dq, kc, vc, sl = W.decode_inputs(wd)
+    times, flops = [], []
+    dec_bytes, dec_secs = 0, 0.0
+    for step in range(args.warmup + args.steps):
+        h = step % w.Hq
+        f, dt = oracle_prefill_sample(w, q, k, v, h, w.Nq - 512, w.Nq)
+        nb, ddt = oracle_decode_sample(wd, dq, kc, vc, sl, [step % wd.B])
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(f)
+            dec_bytes += nb
+            dec_secs += ddt
+    value = sum(flops) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "decode_workload": wd.name,
+                   "sample_per_step": "512 heaviest query rows of one head (prefill) + one sequence (decode)"},
+        "decode": {"value": dec_bytes / dec_secs / 1e9, "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"per step: query rows [{w.Nq - 512}, {w.Nq}) of one head of {w.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, w, wd):
+    from exact_scaled_dot_03_b300 import binding
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    q_h, k_h, v_h = W.prefill_inputs(w)
+    dq_h, kc_h, vc_h, sl_h = W.decode_inputs(wd)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+    dq, kc, vc, sl = dq_h.to(dev), kc_h.to(dev), vc_h.to(dev), sl_h.to(dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty(wd.B, wd.Hq, dtype=torch.float32, device=dev)
+    ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+
+    def decode():
+        binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do, lse=dlse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill()
+        flush.zero_()
+        decode()
+    torch.cuda.synchronize()
+    code, detail = binding.device_status()
+    if code != binding.OK:
+        raise RuntimeError(f"device status after warm-up: {code} {detail}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        prefill()
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        decode()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    launches = 2 * args.steps
+    code, detail = binding.device_status()
+    if code != binding.OK:
+        raise RuntimeError(f"device status after the timed steps: {code} {detail}")
+
+    tot_pre, tot_dec = sum(pre_ms), sum(dec_ms)
+    if world > 1:
+        t = torch.tensor([tot_pre, tot_dec], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_pre, tot_dec = t.tolist()
+
+    flops = w.flops()
+    dec_bytes = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
+    value = world * flops * args.steps / (tot_pre / 1e3) / 1e12
+    dec_value = world * dec_bytes * args.steps / (tot_dec / 1e3) / 1e9
+    peaks = measured_peaks()
+    avg_pre_s = statistics.mean(pre_ms) / 1e3
+    avg_dec_s = statistics.mean(dec_ms) / 1e3
+    achieved = flops / avg_pre_s / 1e12
+    dec_achieved = dec_bytes / avg_dec_s / 1e9
+    fwd_files = ("fwd_kernel.cuh", "ptx.cuh")
+    dec_files = ("decode_kernel.cuh", "ptx.cuh")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                      if peaks.get("bf16_tflops_sustained") else None),
+                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                "traffic": profiled_traffic("attn_fwd_kernel_causal_gqa_traffic.txt", fwd_files),
+                "algorithmic_flops_per_launch": flops, "kernel": "attn_fwd_kernel<128>"}
+    dec_roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
+                "traffic": profiled_traffic("attn_decode_kernel_gqa_traffic.txt", dec_files),
+                "algorithmic_bytes_per_launch": dec_bytes, "kernel": "attn_decode_kernel<128,4>"}
+
+    e2e = None
+    if not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
+        e2e = measure_e2e(args, w, q_h, k_h, v_h, dev)
+        e2e["value"] *= world
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q_h, k_h, v_h)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": (tot_pre + tot_dec) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": w.name, "decode_workload": wd.name,
+                       "l2": "flushed (256 MiB write) before every timed launch",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "prefill_ms": tot_pre / args.steps,
+            "decode": {"metric": "decode GB/s (cache rows read + q/o/lse)", "value": dec_value, "unit": "GB/s",
+                       "ms": tot_dec / args.steps, "roofline": dec_roof},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * world,
+            "clocks": clocks,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(args, w, q_h, k_h, v_h, dev):
+    """Prefill through the public API from pinned host buffers: per step the
+    H2D copy of q, k, v, the launch, and the D2H copy of o and lse."""
+    from exact_scaled_dot_03_b300 import binding as B
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    op = torch.empty_like(q_h).pin_memory()
+    lp = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(qp, device=dev), torch.empty_like(kp, device=dev), torch.empty_like(vp, device=dev)
+    od = torch.empty_like(qd)
+    ld = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+    steps = max(1, min(args.steps, 10))
+
+    def step():
+        qd.copy_(qp, non_blocking=True)
+        kd.copy_(kp, non_blocking=True)
+        vd.copy_(vp, non_blocking=True)
+        B.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld)
+        op.copy_(od, non_blocking=True)
+        lp.copy_(ld, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = (qp.numel() + kp.numel() + vp.numel()) * 2
+    d2h = op.numel() * 2 + lp.numel() * 4
+    return {"value": w.flops() / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    w = PREFILL[args.prefill]
+    wd = W.DECODE_GQA
+    if args.impl == "reference":
+        run_reference(args, w, wd)
+    else:
+        run_ours(args, w, wd)
+
+
+if __name__ == "__main__":
+    main()
