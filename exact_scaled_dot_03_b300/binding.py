@@ -30,6 +30,7 @@ SIGNATURES = {
     "attn_score_bytes": (_u64, [_i64, _i64, _i]),
     "attn_kv_cache_bytes": (_u64, [_i64, _i64, _i64, _i64, _i]),
     "attn_version": (ctypes.c_char_p, []),
+    "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
 }
 
 _lib = None

@@ -298,3 +298,56 @@ uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_
 const char* attn_version(void) { return "exact-attn-sm103 0.1"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory (see
+// attn_decode_noalloc in attn.h). The split-KV scratch that attn_decode takes
+// as a caller workspace lives here instead, in one file-scope device array.
+// Host code must not hand g_noalloc_scratch itself to a kernel: on the host
+// that name is only a stand-in for the symbol, not a device address. The
+// address is looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+void* noalloc_scratch_ptr(int dev) {
+  static void* ptrs[kMaxDevices] = {};
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                                           int Lmax, int d, float scale, void* stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seqlens == nullptr || o == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(seqlens, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  if (!plan_decode(B, Hq, Hkv, Lmax, d, &plan)) return ATTN_ERR_UNSUPPORTED;
+  if (plan.total > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;  // does not fit the static scratch
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  void* scratch = noalloc_scratch_ptr(dev);
+  if (scratch == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The tickets must start at zero; clear them in stream order (no allocation).
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + plan.ticket_off, 0, plan.total - plan.ticket_off, s) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (d == 64)
+    return dispatch_decode_gc<64>(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, scratch, plan, s,
+                                  dev);
+  return dispatch_decode_gc<128>(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, scratch, plan, s,
+                                 dev);
+}

@@ -134,6 +134,41 @@ ATTN_API uint64_t attn_score_bytes(int64_t n, int64_t heads, int bytes_per_score
  * equation; [PW] §3.2). */
 ATTN_API uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_h, int bytes_per_scalar);
 
+/*
+ * Decode without any caller-provided or library-allocated device memory.
+ *
+ * The paper has no counterpart for this entry point; it exists for callers
+ * that cannot call cudaMalloc or hand over a workspace: for example code
+ * running where allocation is forbidden or unsafe (inside a custom allocator
+ * or memory-pool callback, under a framework that owns all device memory, or
+ * at a point where an allocation could trigger a synchronising garbage
+ * collection or fail under memory pressure).
+ *
+ * It computes exactly what attn_decode computes (same arguments, minus the
+ * workspace), but the split-KV scratch lives in one static device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES bytes inside this library. Every GPU that loads
+ * the library holds that array until the process exits.
+ *
+ *   - The caller still passes q, the caches, seqlens, o and (optionally) lse.
+ *   - Returns ATTN_ERR_UNSUPPORTED when the problem would need more scratch
+ *     than the array holds, i.e. when
+ *     attn_decode_workspace_size(B, Hq, Hkv, Lmax, d) > ATTN_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, and it keeps the last call's contents:
+ *     each call first clears the part that must start at zero, on `stream`.
+ *     Calls whose work overlaps on the GPU (different streams, or different
+ *     host threads on the same device) race on the array and must be
+ *     serialised by the caller.
+ *   - Nothing is allocated or freed: no cudaMalloc, no cudaFree, no library
+ *     routine that allocates.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+ATTN_API attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                                         int Lmax, int d, float scale, void* stream);
+
 /* Library version string, e.g. "exact-attn-sm103 0.1". */
 ATTN_API const char* attn_version(void);
 
