@@ -1,13 +1,15 @@
 """Benchmark: exact causal attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--prefill NAME] [--no-cpu-baseline] [--no-e2e]
+                    [--prefill NAME] [--only prefill|decode] [--no-cpu-baseline] [--no-e2e]
 
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
 already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
 N=16384, d=128) followed by a decode step (B=16, Hq=32, Hkv=8, d=128, cache
 lengths uniform on [1024, 8192]). L2 is flushed (a 256 MiB write) before each
-of the two launches, outside their CUDA-event brackets. Prints one JSON line.
+of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
+read so the timed kernel does not pay for writing back the flush's dirty lines.
+Prints one JSON line.
 
 ``value`` is prefill TFLOP/s (4*B*Hq*Nq*Nk*d, halved for causal) over the
 prefill launches; the decode result sits in ``decode`` (GB/s of the cache
@@ -90,7 +92,7 @@ def profiled_traffic(profile_name, files):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -105,7 +107,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
@@ -242,120 +244,135 @@ def run_ours(args, w, wd):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    do_pre = args.only in (None, "prefill")
+    do_dec = args.only in (None, "decode")
 
-    q_h, k_h, v_h = W.prefill_inputs(w)
-    dq_h, kc_h, vc_h, sl_h = W.decode_inputs(wd)
-    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
-    dq, kc, vc, sl = dq_h.to(dev), kc_h.to(dev), vc_h.to(dev), sl_h.to(dev)
-    do = torch.empty_like(dq)
-    dlse = torch.empty(wd.B, wd.Hq, dtype=torch.float32, device=dev)
-    ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
+    parts = []  # (name, launch function)
+    if do_pre:
+        q_h, k_h, v_h = W.prefill_inputs(w)
+        q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+        parts.append(("prefill", lambda: binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)))
+    if do_dec:
+        dq_h, kc_h, vc_h, sl_h = W.decode_inputs(wd)
+        dq, kc, vc, sl = dq_h.to(dev), kc_h.to(dev), vc_h.to(dev), sl_h.to(dev)
+        do = torch.empty_like(dq)
+        dlse = torch.empty(wd.B, wd.Hq, dtype=torch.float32, device=dev)
+        ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
+        parts.append(("decode", lambda: binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do,
+                                                       lse=dlse)))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean_sum = torch.empty((), dtype=torch.float32, device=dev)
 
-    def prefill():
-        binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
-
-    def decode():
-        binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do, lse=dlse)
+    def flush_l2():
+        # Write a buffer larger than L2 (evicts the inputs), then read another
+        # one so that no dirty line is left for the timed kernel to write back.
+        flush.zero_()
+        torch.sum(clean, dim=0, out=clean_sum)
 
     for _ in range(args.warmup):
-        flush.zero_()
-        prefill()
-        flush.zero_()
-        decode()
+        for _, fn in parts:
+            flush_l2()
+            fn()
     torch.cuda.synchronize()
     code, detail = binding.device_status()
     if code != binding.OK:
         raise RuntimeError(f"device status after warm-up: {code} {detail}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+          for _ in range(args.steps)]
     sampler = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
+    # Keep the device busy while the host queues the timed launches, so no
+    # event bracket contains host launch latency (that is the e2e number's job).
+    torch.cuda._sleep(int(2e9 * (0.01 + 0.0004 * args.steps * len(parts))))
     t_wall = time.perf_counter()
-    for e in ev:
-        flush.zero_()
-        e[0].record(stream)
-        prefill()
-        e[1].record(stream)
-        flush.zero_()
-        e[2].record(stream)
-        decode()
-        e[3].record(stream)
+    for step in ev:
+        for (e0, e1), (_, fn) in zip(step, parts):
+            flush_l2()           # outside the event bracket
+            e0.record(stream)
+            fn()
+            e1.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    launches = 2 * args.steps
+    ms = {name: [step[i][0].elapsed_time(step[i][1]) for step in ev] for i, (name, _) in enumerate(parts)}
+    launches = len(parts) * args.steps
     code, detail = binding.device_status()
     if code != binding.OK:
         raise RuntimeError(f"device status after the timed steps: {code} {detail}")
 
-    tot_pre, tot_dec = sum(pre_ms), sum(dec_ms)
+    tot = {name: sum(v) for name, v in ms.items()}
     if world > 1:
-        t = torch.tensor([tot_pre, tot_dec], dtype=torch.float64, device=dev)
+        t = torch.tensor([tot[n] for n, _ in parts], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_pre, tot_dec = t.tolist()
-
-    flops = w.flops()
-    dec_bytes = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
-    value = world * flops * args.steps / (tot_pre / 1e3) / 1e12
-    dec_value = world * dec_bytes * args.steps / (tot_dec / 1e3) / 1e9
+        tot = {n: x for (n, _), x in zip(parts, t.tolist())}
     peaks = measured_peaks()
-    avg_pre_s = statistics.mean(pre_ms) / 1e3
-    avg_dec_s = statistics.mean(dec_ms) / 1e3
-    achieved = flops / avg_pre_s / 1e12
-    dec_achieved = dec_bytes / avg_dec_s / 1e9
-    fwd_files = ("fwd_kernel.cuh", "ptx.cuh")
-    dec_files = ("decode_kernel.cuh", "ptx.cuh")
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
-                "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
-                                      if peaks.get("bf16_tflops_sustained") else None),
-                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                "traffic": profiled_traffic("attn_fwd_kernel_causal_gqa_traffic.txt", fwd_files),
-                "algorithmic_flops_per_launch": flops, "kernel": "attn_fwd_kernel<128>"}
-    dec_roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dec_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
-                "traffic": profiled_traffic("attn_decode_kernel_gqa_traffic.txt", dec_files),
-                "algorithmic_bytes_per_launch": dec_bytes, "kernel": "attn_decode_kernel<128,4>"}
+
+    roofline = dec_block = None
+    value = unit = None
+    if do_pre:
+        flops = w.flops()
+        value = world * flops * args.steps / (tot["prefill"] / 1e3) / 1e12
+        unit = "TFLOP/s"
+        achieved = flops / (statistics.mean(ms["prefill"]) / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"],
+                    "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                          if peaks.get("bf16_tflops_sustained") else None),
+                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                    "traffic": profiled_traffic("attn_fwd_kernel_causal_gqa_traffic.txt",
+                                                ("fwd_kernel.cuh", "ptx.cuh")),
+                    "algorithmic_flops_per_launch": flops, "kernel": "attn_fwd_kernel<128>"}
+    if do_dec:
+        dec_bytes = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
+        dec_value = world * dec_bytes * args.steps / (tot["decode"] / 1e3) / 1e9
+        dec_achieved = dec_bytes / (statistics.mean(ms["decode"]) / 1e3) / 1e9
+        dec_roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": dec_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
+                    "traffic": profiled_traffic("attn_decode_kernel_gqa_traffic.txt",
+                                                ("decode_kernel.cuh", "ptx.cuh")),
+                    "algorithmic_bytes_per_launch": dec_bytes, "kernel": "attn_decode_kernel<128,4>"}
+        dec_block = {"metric": "decode GB/s (cache rows read + q/o/lse)", "value": dec_value, "unit": "GB/s",
+                     "ms": tot["decode"] / args.steps, "roofline": dec_roof}
+        if not do_pre:   # decode alone: its numbers are the line's
+            value, unit, roofline = dec_value, "GB/s", dec_roof
 
     e2e = None
-    if not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
+    if do_pre and not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
         e2e = measure_e2e(args, w, q_h, k_h, v_h, dev)
         e2e["value"] *= world
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if do_pre and rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q_h, k_h, v_h)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": (tot_pre + tot_dec) / args.steps,
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sum(tot.values()) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16)",
-            "config": {"workload": w.name, "decode_workload": wd.name,
-                       "l2": "flushed (256 MiB write) before every timed launch",
+            "config": {"workload": w.name if do_pre else wd.name,
+                       "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "prefill_ms": tot_pre / args.steps,
-            "decode": {"metric": "decode GB/s (cache rows read + q/o/lse)", "value": dec_value, "unit": "GB/s",
-                       "ms": tot_dec / args.steps, "roofline": dec_roof},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches * world,
-            "clocks": clocks,
-            "wall_s_timed_region": t_wall,
         }
+        if do_pre and do_dec:
+            line["config"]["decode_workload"] = wd.name
+        if do_pre:
+            line["prefill_ms"] = tot["prefill"] / args.steps
+        if do_pre and do_dec:
+            line["decode"] = dec_block
+        line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
+                     "clocks": clocks, "wall_s_timed_region": t_wall})
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -400,12 +417,14 @@ def measure_e2e(args, w, q_h, k_h, v_h, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -122,9 +122,14 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, flo
 }
 
 struct DecodePlan {
-  int G, GC, qgroups, units, split, max_splits;
+  int G, GC, qgroups, units, slots;
   size_t part_o_off, part_lse_off, ticket_off, total;
 };
+
+// Keys per decode tile and the minimum chunk (in tiles) a CTA takes; both
+// must match DecCfg in decode_kernel.cuh.
+constexpr int kDecTile = 128;
+constexpr int kDecMinChunk = 4;
 
 bool plan_decode(int B, int Hq, int Hkv, int Lmax, int d, DecodePlan* p) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return false;
@@ -133,16 +138,28 @@ bool plan_decode(int B, int Hq, int Hkv, int Lmax, int d, DecodePlan* p) {
   p->GC = p->G % 8 == 0 ? 8 : p->G % 4 == 0 ? 4 : p->G % 2 == 0 ? 2 : 1;
   p->qgroups = p->G / p->GC;
   const long long units = static_cast<long long>(B) * Hkv * p->qgroups;
-  if (units > 65535) return false;
+  if (units > (1 << 24)) return false;
   p->units = static_cast<int>(units);
-  p->split = 512;  // keys per CTA; a multiple of the 64-key tile
-  p->max_splits = (Lmax + p->split - 1) / p->split;
-  const size_t slots = static_cast<size_t>(p->units) * p->max_splits * p->GC;
+  // A unit of n tiles is cut into at most ceil(n / chunk) + 1 pieces, and a
+  // chunk is never shorter than kDecMinChunk tiles.
+  const long long tiles = (static_cast<long long>(Lmax) + kDecTile - 1) / kDecTile;
+  p->slots = static_cast<int>((tiles + kDecMinChunk - 1) / kDecMinChunk + 1);
+  const size_t slots = static_cast<size_t>(p->units) * p->slots * p->GC;
   p->part_o_off = 0;
   p->part_lse_off = slots * d * sizeof(float);
   p->ticket_off = p->part_lse_off + ((slots * sizeof(float) + 15) & ~size_t(15));
   p->total = p->ticket_off + ((static_cast<size_t>(p->units) * sizeof(int) + 15) & ~size_t(15));
   return true;
+}
+
+int sm_count(int dev) {
+  static int counts[kMaxDevices] = {};
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
 }
 
 template <int D, int GC>
@@ -171,12 +188,13 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
   a.Lmax = Lmax;
   a.group = plan.G;
   a.qgroups = plan.qgroups;
-  a.split = plan.split;
-  a.max_splits = plan.max_splits;
+  a.slots = plan.slots;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = status_ptr(dev);
   if (a.status == nullptr) return ATTN_ERR_CUDA;
-  dim3 grid(plan.max_splits, plan.units);
+  static_assert(C::TK == kDecTile && C::MIN_CHUNK == kDecMinChunk, "decode plan and kernel disagree");
+  const int grid = sm_count(dev);  // persistent: one CTA per SM
+  if (grid == 0) return ATTN_ERR_CUDA;
   attn_decode_kernel<D, GC><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

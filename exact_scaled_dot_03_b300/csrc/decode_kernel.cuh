@@ -6,15 +6,41 @@
 // [PW] pwwt.cn news 6124947; [MG-A] menggq.pages.dev "Transformer 架构的数学与
 // 计算深度解析" (§6.3, two-block merge); [AUT] auturnal.com "从注意力到 IO 感知执行" (§8).
 //
-// The work is bound by reading the cache, so it runs on the CUDA cores: the
-// contraction per key is only GC x D multiply-adds for 2*D*2 bytes read.
-// Grid: (split, (b, kv head, query group)). Each CTA streams its split of the
-// cache through a ring of TMA-loaded 64-key tiles (128-byte swizzled, so the
-// per-key row reads below are bank-conflict free), keeps the blockwise softmax
-// statistics (m, l, un-normalised u) of [AUT] §8 for each of its GC query
-// heads, and writes a partial (o = u / l, lse). The last CTA of a
-// (b, kv head, query group) to finish merges the partials with the two-block
-// rule of [MG-A] §6.3 generalised to n blocks, and resets its ticket.
+// The work is bound by reading the cache. Its two contractions per KV head
+// are small dense products (GC query heads x 16 keys x D per warp and tile);
+// on the CUDA cores their issue cost (unpacking bf16, cross-lane sums) kept
+// the kernel from saturating HBM, so they run as warp-level tensor-core MMAs
+// (m16n8k16, bf16 in, fp32 accumulate) on fragments read with ldmatrix from
+// the TMA-staged tiles; the kernel stays bound by the cache read.
+//
+// Work split (persistent, balanced). A "unit" is one (sequence b, KV head,
+// group of GC query heads); its cache rows are cut into 128-key tiles. All
+// units' tiles are laid end to end (sequence-major) and the grid (one CTA per
+// SM) takes equal contiguous chunks of that list, so every CTA streams the
+// same number of bytes whatever the length mix. A chunk covers the tail of
+// one unit, whole units, and the head of another; each such "piece" ends in a
+// result (o = u / l and its log-sum-exp). A unit covered by one piece is
+// written out directly. Otherwise the piece is a partial result (at most two
+// per CTA: its first and its last piece); once a CTA has streamed all its
+// tiles it takes a ticket for each, and the last piece of a unit to finish
+// merges the partials with the two-block rule of [MG-A] §6.3 generalised to
+// n blocks, and resets the ticket.
+//
+// Inside a CTA: K and V tiles stream through a ring of STAGES TMA-loaded
+// shared-memory stages (128-byte swizzle). Warp w owns keys [16 w, 16 w + 16)
+// of every tile and keeps its own blockwise-softmax state ([AUT] §8: running
+// max m, denominator l, un-normalised u) for the GC query heads, so no
+// CTA-wide barrier is needed per tile; the last warp to finish with a stage
+// refills it (a per-stage release counter, no producer warp). At the end of a
+// piece every warp leaves its (m, l, u) in shared memory and, after one
+// barrier, each thread merges two output elements over the warps (max,
+// rescale, sum); the next piece's query fragments are loaded meanwhile.
+//
+// Per warp and tile: S = Q K^T as 2 x D/16 MMAs (query rows 0..GC-1 of the
+// 16-row A operand; the rest are zero), the scale applied in fp32, the
+// running max moved lazily (only when a tile's max exceeds it by more than 8
+// in base-2 units; l and u always share it, so o = u / l is unchanged), P
+// rounded to bf16 and fed back as the A operand of O += P V (D/8 MMAs).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -29,14 +55,13 @@ struct DecArgs {
   const int* seqlens;      // [B]
   __nv_bfloat16* o;        // [B, Hq, D]
   float* lse;              // [B, Hq] natural-log LSE, or nullptr
-  float* part_o;           // [units][max_splits][GC][D]   (workspace)
-  float* part_lse;         // [units][max_splits][GC]      (workspace, base-2 units)
-  int* tickets;            // [units]                      (workspace, zero between calls)
+  float* part_o;           // [units][slots][GC][D]   (workspace) normalised partial outputs
+  float* part_lse;         // [units][slots][GC]      (workspace) partial LSE, base-2 units
+  int* tickets;            // [units]                 (workspace, zero between calls)
   int B, Hq, Hkv, Lmax;
   int group;               // Hq / Hkv
   int qgroups;             // group / GC
-  int split;               // keys per split (multiple of 64)
-  int max_splits;          // ceil(Lmax / split)
+  int slots;               // partial slots per unit (>= pieces any unit can be cut into)
   float scale_log2;        // scale * log2(e)
   unsigned* status;
 };
@@ -44,302 +69,452 @@ struct DecArgs {
 template <int D, int GC>
 struct DecCfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(GC == 1 || GC == 2 || GC == 4 || GC == 8, "query heads per CTA");
-  static constexpr int THREADS = 256;
-  static constexpr int TK = 64;                      // keys per tile
-  static constexpr int KBLK = D / 64;                // 128-byte swizzle blocks per row
-  static constexpr int BOX_BYTES = TK * 64 * 2;      // 64 keys x 64 columns
+  static_assert(GC == 1 || GC == 2 || GC == 4 || GC == 8, "query heads per unit");
+  static constexpr int NW = 8;                   // warps; every warp consumes, any warp may refill
+  static constexpr int THREADS = NW * 32;
+  static constexpr int TK = 128;                 // keys per tile
+  static constexpr int KPW = TK / NW;            // keys per warp per tile (one 16-key MMA step)
+  static_assert(KPW == 16, "one k-step of the P.V MMA per warp");
+  static constexpr int KBLK = D / 64;            // 64-column (128-byte) swizzle boxes per row
+  static constexpr int BOX_BYTES = TK * 128;
   static constexpr int TILE_BYTES = KBLK * BOX_BYTES;  // K (or V) tile
-  static constexpr int STAGES = 3;
-  static constexpr int KV_OFF = 0;                   // stage s: K at 2s, V at 2s+1
-  static constexpr int Q_OFF = KV_OFF + STAGES * 2 * TILE_BYTES;
-  static constexpr int S_OFF = Q_OFF + GC * D * 4;   // scores [GC][TK]
-  static constexpr int P_OFF = S_OFF + GC * TK * 4;  // probabilities [TK][GC]
-  static constexpr int A_OFF = P_OFF + GC * TK * 4;  // alpha [GC], m [GC], l [GC]
-  static constexpr int BAR_OFF = A_OFF + 3 * 8 * 4;
-  static constexpr int MISC_OFF = BAR_OFF + STAGES * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
-  // cross-warp reduction of the value accumulators reuses the K/V ring
-  static_assert(8 * GC * D * 4 <= STAGES * 2 * TILE_BYTES, "reduction scratch");
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K then V
+  static constexpr int STAGES = (D == 128) ? 3 : 6;
+  static constexpr int MIN_CHUNK = 4;            // tiles: bounds the pieces a unit is cut into
+  // shared memory
+  static constexpr int RING_OFF = 0;
+  static constexpr int SL_OFF = RING_OFF + STAGES * STAGE_BYTES;  // [NW][GC][D] per-warp u
+  static constexpr int WM_OFF = SL_OFF + NW * GC * D * 4;         // [NW][GC] per-warp running max
+  static constexpr int WL_OFF = WM_OFF + NW * GC * 4;             // [NW][GC] per-warp denominator
+  static constexpr int BAR_OFF = WL_OFF + NW * GC * 4;            // full[STAGES]
+  static constexpr int CNT_OFF = BAR_OFF + STAGES * 8;            // releases[STAGES], fills[STAGES]
+  static constexpr int MISC_OFF = CNT_OFF + 2 * STAGES * 4 + 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 64 + 1024;         // + alignment slack
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Position in the CTA's tile list: sequence b (nt tiles per unit, list offset
+// P of its first unit), unit r within the sequence, tile j within the unit.
+struct TileCursor {
+  int b, nt, r, j;
+  long long P;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Cache length of sequence b, clamped into [0, Lmax].
+__device__ __forceinline__ int dec_len(const DecArgs& a, int b) {
+  const int L = a.seqlens[b];
+  return max(0, min(L, a.Lmax));
+}
+
+// Sum of x over the warp (all lanes receive it).
+__device__ __forceinline__ long long warp_sum_ll(long long x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Wait sites recorded in status[1] when a bounded wait gives up.
+enum : unsigned { kSiteDecFull = 20, kSiteDecDrain = 22 };
+
+template <int TK>
+__device__ __forceinline__ int dec_tiles(const DecArgs& a, int b) {
+  return (dec_len(a, b) + TK - 1) / TK;
+}
+
+// Steps a cursor to the next tile in list order. Only called while a later
+// tile exists, so the loop over empty sequences stops inside [0, B).
+template <int TK>
+__device__ __forceinline__ void dec_advance(const DecArgs& a, int UPB, TileCursor& c) {
+  if (++c.j < c.nt) return;
+  c.j = 0;
+  if (++c.r < UPB) return;
+  c.r = 0;
+  c.P += (long long)c.nt * UPB;
+  do {
+    ++c.b;
+    c.nt = dec_tiles<TK>(a, c.b);
+  } while (c.nt == 0);
+}
+
 template <int D, int GC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const DecArgs a) {
   using C = DecCfg<D, GC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* q_s = reinterpret_cast<float*>(smem + C::Q_OFF);   // [GC][D], pre-scaled by scale*log2(e)
-  float* s_s = reinterpret_cast<float*>(smem + C::S_OFF);   // [GC][TK]
-  float* p_s = reinterpret_cast<float*>(smem + C::P_OFF);   // [TK][GC]
-  float* alpha_s = reinterpret_cast<float*>(smem + C::A_OFF);
-  float* m_s = alpha_s + 8;
-  float* l_s = alpha_s + 16;
+  uint8_t* ring = smem + C::RING_OFF;
+  float* sl_sm = reinterpret_cast<float*>(smem + C::SL_OFF);
+  float* wm_sm = reinterpret_cast<float*>(smem + C::WM_OFF);
+  float* wl_sm = reinterpret_cast<float*>(smem + C::WL_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  int* flag_s = reinterpret_cast<int*>(smem + C::MISC_OFF);
+  int* releases = reinterpret_cast<int*>(smem + C::CNT_OFF);  // warps done with each stage (monotonic)
+  int* fills = releases + C::STAGES;                          // loads issued into each stage
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
+  volatile int* last_flag = abort_flag + 1;
+  long long* plan_sm = reinterpret_cast<long long*>(smem + C::MISC_OFF + 16);  // T, b_start, P_start
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int split_idx = blockIdx.x;
-  const int unit = blockIdx.y;                  // (b, hkv, qg)
-  const int qg = unit % a.qgroups;
-  const int bh = unit / a.qgroups;
-  const int hkv = bh % a.Hkv;
-  const int b = bh / a.Hkv;
-  const int h0 = hkv * a.group + qg * GC;       // first query head of this CTA
-
-  int L = a.seqlens[b];
-  if (L < 0 || L > a.Lmax) {
-    if (split_idx == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
-    L = max(0, min(L, a.Lmax));
-  }
-  const int n_splits = (L + a.split - 1) / a.split;
-  if (L == 0) {
-    // No cached key: o = 0, lse = -inf.
-    if (split_idx == 0) {
-      for (int i = tid; i < GC * D; i += C::THREADS)
-        a.o[(size_t)(b * a.Hq + h0 + i / D) * D + i % D] = __float2bfloat16_rn(0.f);
-      if (a.lse != nullptr && tid < GC) a.lse[b * a.Hq + h0 + tid] = -CUDART_INF_F;
-    }
-    return;
-  }
-  if (split_idx >= n_splits) return;
-  const int k_begin = split_idx * a.split;
-  const int k_end = min(L, k_begin + a.split);
-  const int n_tiles = (k_end - k_begin + C::TK - 1) / C::TK;
+  const int UPB = a.Hkv * a.qgroups;  // units per sequence
 
   if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(full + s, 1);
-    *flag_s = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);
+      releases[s] = 0;
+      fills[s] = 0;
+    }
+    *abort_flag = 0;
+    *last_flag = 0;
     fence_mbarrier_init();
   }
-  for (int i = tid; i < GC * D; i += C::THREADS) {
-    const float qv = __bfloat162float(a.q[(size_t)(b * a.Hq + h0 + i / D) * D + i % D]);
-    q_s[i] = qv * a.scale_log2;
+
+  // ---- the tile list: total T, and the sequence this CTA's chunk starts in
+  if (warp == 0) {
+    bool bad = false;
+    long long total = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      const int b = b0 + lane;
+      long long tiles = 0;
+      if (b < a.B) {
+        const int L = a.seqlens[b];
+        bad |= (L < 0 || L > a.Lmax);
+        tiles = (long long)((max(0, min(L, a.Lmax)) + C::TK - 1) / C::TK) * UPB;
+      }
+      total += warp_sum_ll(tiles);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad && blockIdx.x == 0 && lane == 0) atomicOr(a.status, kStatusBadSeqlen);
+    const long long chunk = max((total + gridDim.x - 1) / gridDim.x, (long long)C::MIN_CHUNK);
+    const long long t0 = (long long)blockIdx.x * chunk;
+    if (lane == 0) {
+      plan_sm[0] = total;
+      plan_sm[1] = -1;
+      plan_sm[2] = 0;
+    }
+    __syncwarp();
+    if (t0 < total) {
+      long long run = 0;
+      for (int b0 = 0; b0 < a.B && run <= t0; b0 += 32) {
+        const int b = b0 + lane;
+        const long long tiles = b < a.B ? (long long)dec_tiles<C::TK>(a, b) * UPB : 0;
+        long long incl = tiles;  // inclusive warp scan
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const long long lo = run + incl - tiles;
+        if (tiles > 0 && t0 >= lo && t0 < lo + tiles) {
+          plan_sm[1] = b;
+          plan_sm[2] = lo;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
   }
   __syncthreads();
 
-  auto issue = [&](int tile) {
-    const int s = tile % C::STAGES;
-    uint8_t* kdst = smem + C::KV_OFF + (2 * s) * C::TILE_BYTES;
+  // Sequences with no cached key: o = 0, lse = -inf.
+  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+    if (dec_len(a, b) != 0) continue;
+    for (int i = tid; i < a.Hq * D; i += C::THREADS)
+      a.o[(size_t)b * a.Hq * D + i] = __float2bfloat16_rn(0.f);
+    if (a.lse != nullptr)
+      for (int i = tid; i < a.Hq; i += C::THREADS) a.lse[(size_t)b * a.Hq + i] = -CUDART_INF_F;
+  }
+
+  const long long T = plan_sm[0];
+  const long long chunk = max((T + gridDim.x - 1) / gridDim.x, (long long)C::MIN_CHUNK);
+  const long long t0 = (long long)blockIdx.x * chunk;
+  if (t0 >= T) return;  // uniform over the CTA
+  const long long t1 = min(T, t0 + chunk);
+  const int n_tiles = static_cast<int>(t1 - t0);
+
+  TileCursor cur;
+  cur.b = static_cast<int>(plan_sm[1]);
+  cur.P = plan_sm[2];
+  cur.nt = dec_tiles<C::TK>(a, cur.b);
+  cur.r = static_cast<int>((t0 - cur.P) / cur.nt);
+  cur.j = static_cast<int>((t0 - cur.P) % cur.nt);
+
+  // Loads tile `c` into stage s (one thread).
+  auto issue = [&](const TileCursor& c, int s) {
+    uint8_t* kdst = ring + s * C::STAGE_BYTES;
     uint8_t* vdst = kdst + C::TILE_BYTES;
-    mbar_arrive_expect_tx(full + s, 2 * C::TILE_BYTES);
-    const int key = k_begin + tile * C::TK;
+    const int plane = c.b * a.Hkv + c.r / a.qgroups;
+    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
 #pragma unroll
     for (int kb = 0; kb < C::KBLK; ++kb) {
-      tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, key, b * a.Hkv + hkv);
-      tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, key, b * a.Hkv + hkv);
+      tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, c.j * C::TK, plane);
+      tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, c.j * C::TK, plane);
+    }
+    fills[s] += 1;
+  };
+
+  // The first STAGES tiles are issued up front; after that, the last warp to
+  // release a stage refills it with the tile STAGES further on (`ahead`).
+  TileCursor ahead = cur;
+  for (int k = 0; k < C::STAGES && k < n_tiles; ++k) {
+    if (tid == 0) {
+      if (k == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
+      issue(ahead, k);
+    }
+    if (k + 1 < n_tiles) dec_advance<C::TK>(a, UPB, ahead);
+  }
+
+  // Fragment coordinates (m16n8k16): lane = 4 g + t holds query row g and
+  // key / value columns 2t, 2t+1 of each 8-wide n-tile.
+  const int g = lane >> 2;
+  const int t4 = lane & 3;
+  const bool row_live = g < GC;
+  // ldmatrix row addresses: lane i feeds row (i % 8) of matrix (i / 8).
+  const int lm_mat = lane >> 3;
+  const int lm_row = lane & 7;
+  const float sl2 = a.scale_log2;
+
+  // Q of a unit as the A operand (rows >= GC are zero): qa[kk] = {a0, a2} of k-step kk.
+  auto load_q = [&](const TileCursor& c, uint32_t (&qa)[D / 16][2]) {
+    const int h0 = (c.r / a.qgroups) * a.group + (c.r % a.qgroups) * GC;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(a.q + ((size_t)c.b * a.Hq + h0 + (row_live ? g : 0)) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = row_live ? qrow[kk * 8 + t4] : 0u;
+      qa[kk][1] = row_live ? qrow[kk * 8 + 4 + t4] : 0u;
     }
   };
-  int issued = 0;  // tiles whose loads thread 0 has issued
-  if (tid == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    for (int t = 0; t < C::STAGES - 1 && t < n_tiles; ++t) issue(t), ++issued;
-  }
+  uint32_t qa[D / 16][2];
+  load_q(cur, qa);
 
-  // QK mapping: thread -> (key within tile, query subset)
-  const int qk_key = tid & (C::TK - 1);
-  const int qk_sel = tid >> 6;                       // 0..3, warp-uniform
-  constexpr int QPT = GC >= 4 ? GC / 4 : 1;          // queries per thread
-  const bool qk_active = GC >= 4 || qk_sel < GC;
-  // PV mapping: warp -> keys w, w+8, ...; lane -> EPL consecutive value columns
-  constexpr int EPL = D / 32;
-  float acc[GC][EPL];
-#pragma unroll
-  for (int g = 0; g < GC; ++g)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
-  float m_run = -CUDART_INF_F, l_run = 0.f;  // owned by warp g (< GC), replicated over its lanes
-  bool ok = true;
+  // Partial pieces of this CTA (its first and/or last), settled after the stream.
+  int pend_n = 0;
+  int pend_u[2], pend_pieces[2], pend_b[2], pend_h0[2];
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const int s = tile % C::STAGES;
-    const uint8_t* ks = smem + C::KV_OFF + (2 * s) * C::TILE_BYTES;
-    const uint8_t* vs = ks + C::TILE_BYTES;
-    if (!mbar_wait(full + s, (tile / C::STAGES) & 1, a.status, 20)) ok = false;
-    if (!ok) *flag_s = 1;
-    const int key0 = k_begin + tile * C::TK;
-    // ---- scores: s[g][key] = (scale*log2e) q_g . k_key
-    if (qk_active) {
-      float dot[QPT];
+  int it_tile = 0;  // tiles of this CTA consumed so far (ring position)
+  while (it_tile < n_tiles) {
+    const int jbeg = cur.j;
+    const int jend = min(cur.nt, jbeg + (n_tiles - it_tile));
+    const int b = cur.b;
+    const int h0 = (cur.r / a.qgroups) * a.group + (cur.r % a.qgroups) * GC;
+    const int L = dec_len(a, b);
+
+    float m_run = -CUDART_INF_F;  // reference max of row g (base-2 units), shared by l and o
+    float l_part = 0.f;           // this lane's share of the denominator of row g
+    float o[D / 8][4];            // O rows g (c0, c1) and g + 8 (c2, c3, always 0)
 #pragma unroll
-      for (int i = 0; i < QPT; ++i) dot[i] = 0.f;
-      const int sw = qk_key & 7;
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    for (int jj = jbeg; jj < jend; ++jj, ++it_tile) {
+      const int s = it_tile % C::STAGES;
+      bool live = !*abort_flag;
+      if (live && !mbar_wait(full + s, (it_tile / C::STAGES) & 1, a.status, kSiteDecFull)) {
+        *abort_flag = 1;
+        live = false;
+      }
+      if (live) {
+        const uint32_t kt = smem_u32(ring + s * C::STAGE_BYTES);
+        const uint32_t vt = kt + C::TILE_BYTES;
+        const int row0 = warp * C::KPW;          // first tile row of this warp
+        const int key0 = jj * C::TK + row0;      // its key index in the sequence
+        // ---- S = Q K^T for this warp's 16 keys: n-tile 0 = keys 0-7, 1 = keys 8-15
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int krow = row0 + (lm_mat >> 1) * 8 + lm_row;
+          const uint32_t kbase = kt + krow * 128;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint8_t* rowp = ks + (c >> 3) * C::BOX_BYTES + qk_key * 128;
-        const uint4 kw = *reinterpret_cast<const uint4*>(rowp + (((c & 7) ^ sw) << 4));
-        float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                       bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = 2 * kk + (lm_mat & 1);
+            uint32_t kb[4];
+            ldsm_x4(kbase + (chunk >> 3) * C::BOX_BYTES + (((chunk & 7) ^ (krow & 7)) << 4), kb);
+            mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, kb[0], kb[1]);
+            mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, kb[2], kb[3]);
+          }
+        }
+        // ---- mask, lazy running max, probabilities (row g; keys 8n + 2t + e)
+        const int nvalid = L - key0;  // keys of this warp below the length
+        float sv[4];
 #pragma unroll
-        for (int i = 0; i < QPT; ++i) {
-          const int g = qk_sel + 4 * i;
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + g * D + 8 * c);
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + g * D + 8 * c + 4);
-          dot[i] = fmaf(qa.x, kf[0], dot[i]);
-          dot[i] = fmaf(qa.y, kf[1], dot[i]);
-          dot[i] = fmaf(qa.z, kf[2], dot[i]);
-          dot[i] = fmaf(qa.w, kf[3], dot[i]);
-          dot[i] = fmaf(qb.x, kf[4], dot[i]);
-          dot[i] = fmaf(qb.y, kf[5], dot[i]);
-          dot[i] = fmaf(qb.z, kf[6], dot[i]);
-          dot[i] = fmaf(qb.w, kf[7], dot[i]);
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            sv[2 * n + e] = (8 * n + 2 * t4 + e < nvalid) ? sacc[n][e] * sl2 : -CUDART_INF_F;
+        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const bool need = mx > m_run + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m_run - mx) : 1.f;  // 0 while m_run is -inf
+          if (need) m_run = mx;
+          l_part *= alpha;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            o[n][0] *= alpha;
+            o[n][1] *= alpha;
+          }
+        }
+        const float m_ref = (m_run == -CUDART_INF_F) ? 0.f : m_run;
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          p[i] = ex2_approx(sv[i] - m_ref);
+          l_part += p[i];
+        }
+        const uint32_t pa0 = pack_bf16x2(p[0], p[1]);  // keys 2t, 2t+1
+        const uint32_t pa2 = pack_bf16x2(p[2], p[3]);  // keys 8+2t, 8+2t+1
+        // ---- rows past the length may hold anything (even NaN): zero them so
+        // that 0 * V stays 0 in the MMA. Only this warp reads its rows.
+        if (nvalid < C::KPW) {
+          for (int i = lane; i < C::KPW * (D / 8); i += 32) {
+            const int r = i / (D / 8), c = i % (D / 8);
+            if (r >= max(nvalid, 0)) {
+              const int row = row0 + r;
+              *reinterpret_cast<uint4*>(ring + s * C::STAGE_BYTES + C::TILE_BYTES + (c >> 3) * C::BOX_BYTES +
+                                        row * 128 + (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();  // before a later TMA refill overwrites these rows
+          __syncwarp();
+        }
+        // ---- O += P V: B fragments of two 8-column n-tiles per ldmatrix
+        {
+          const int vrow = row0 + (lm_mat & 1) * 8 + lm_row;
+          const uint32_t vbase = vt + vrow * 128;
+#pragma unroll
+          for (int jp = 0; jp < D / 16; ++jp) {
+            const int chunk = 2 * jp + (lm_mat >> 1);
+            uint32_t vb[4];
+            ldsm_x4_trans(vbase + (chunk >> 3) * C::BOX_BYTES + (((chunk & 7) ^ (vrow & 7)) << 4), vb);
+            mma_bf16_16816(o[2 * jp], pa0, 0u, pa2, 0u, vb[0], vb[1]);
+            mma_bf16_16816(o[2 * jp + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
+          }
         }
       }
-      const bool valid = key0 + qk_key < k_end;
-#pragma unroll
-      for (int i = 0; i < QPT; ++i) s_s[(qk_sel + 4 * i) * C::TK + qk_key] = valid ? dot[i] : -CUDART_INF_F;
-    }
-    __syncthreads();
-    // Flags are only written before the barrier above, so every thread takes
-    // the same branch here.
-    if (*flag_s) break;
-    // The stage read two tiles ago is free now: refill it.
-    if (tid == 0 && tile + C::STAGES - 1 < n_tiles) issue(tile + C::STAGES - 1), ++issued;
-    // ---- online softmax update, one warp per query head
-    if (warp < GC) {
-      const float s0 = s_s[warp * C::TK + lane];
-      const float s1 = s_s[warp * C::TK + lane + 32];
-      float mx = fmaxf(s0, s1);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float m_new = fmaxf(m_run, mx);       // finite: every tile has a valid key
-      const float alpha = ex2_approx(m_run - m_new);
-      const float p0 = ex2_approx(s0 - m_new);
-      const float p1 = ex2_approx(s1 - m_new);
-      float sum = p0 + p1;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      l_run = l_run * alpha + sum;
-      m_run = m_new;
-      p_s[lane * GC + warp] = p0;
-      p_s[(lane + 32) * GC + warp] = p1;
-      if (lane == 0) alpha_s[warp] = alpha;
-    }
-    __syncthreads();
-    // ---- u = alpha u + sum_k p_k v_k
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      const float al = alpha_s[g];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[g][e] *= al;
-    }
-    const int e0 = lane * EPL;              // first value column of this lane
-    const int vblk = e0 >> 6;               // 64-column swizzle block
-    const int vchunk = (e0 & 63) >> 3;      // 16-byte chunk inside the 128-byte row
-    const int vin = (e0 & 7) * 2;           // byte offset inside the chunk
-    const int n_valid = min(C::TK, k_end - key0);  // rows past the length are never touched
-#pragma unroll 2
-    for (int kk = warp; kk < n_valid; kk += 8) {
-      const uint8_t* rowp = vs + vblk * C::BOX_BYTES + kk * 128 + (((vchunk ^ (kk & 7)) << 4) + vin);
-      float vf[EPL];
-      if constexpr (EPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(rowp);
-        vf[0] = bf16lo(w.x); vf[1] = bf16hi(w.x); vf[2] = bf16lo(w.y); vf[3] = bf16hi(w.y);
-      } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(rowp);
-        vf[0] = bf16lo(w); vf[1] = bf16hi(w);
-      }
-      float pg[GC];
-      if constexpr (GC >= 4) {
-#pragma unroll
-        for (int g4 = 0; g4 < GC; g4 += 4) {
-          const float4 pp = *reinterpret_cast<const float4*>(p_s + kk * GC + g4);
-          pg[g4] = pp.x; pg[g4 + 1] = pp.y; pg[g4 + 2] = pp.z; pg[g4 + 3] = pp.w;
+      __syncwarp();  // this warp's reads of the stage are done
+      if (lane == 0) {
+        __threadfence_block();
+        const int done = atomicAdd(releases + s, 1) + 1;
+        if (done % C::NW == 0) {
+          // Last warp off this stage: refill it with the tile STAGES further on.
+          __threadfence_block();
+          if (it_tile + C::STAGES < n_tiles && !*abort_flag) issue(ahead, s);
         }
-      } else {
-#pragma unroll
-        for (int g = 0; g < GC; ++g) pg[g] = p_s[kk * GC + g];
       }
-#pragma unroll
-      for (int g = 0; g < GC; ++g)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pg[g], vf[e], acc[g][e]);
+      if (it_tile + C::STAGES + 1 < n_tiles) dec_advance<C::TK>(a, UPB, ahead);
     }
-  }
-  __syncthreads();
-  if (*flag_s) {
-    // A wait gave up: let the copies still in flight land, then leave.
-    if (tid == 0)
-      for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-        mbar_wait(full + t % C::STAGES, (t / C::STAGES) & 1, a.status, 21);
-    return;
-  }
-  // Every issued tile was waited on above, so all loads have landed and the
-  // ring is free for the cross-warp reduction.
-  float* red = reinterpret_cast<float*>(smem + C::KV_OFF);  // [8][GC][D]
-#pragma unroll
-  for (int g = 0; g < GC; ++g)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) red[(warp * GC + g) * D + lane * EPL + e] = acc[g][e];
-  if (warp < GC && lane == 0) {
-    m_s[warp] = m_run;
-    l_s[warp] = l_run;
-  }
-  __syncthreads();
 
-  const size_t pbase = (size_t)unit * a.max_splits;
-  if (n_splits == 1) {
+    // ---- end of the piece. Start loading the next piece's queries first.
+    const int u_idx = b * UPB + cur.r;
+    const long long P_u = cur.P + (long long)cur.r * cur.nt;
+    const bool whole = (jbeg == 0 && jend == cur.nt);
+    const int slot = static_cast<int>(blockIdx.x - P_u / chunk);
+    const int pieces = static_cast<int>((P_u + cur.nt - 1) / chunk - P_u / chunk + 1);
+    if (it_tile < n_tiles) {
+      cur.j = jend - 1;
+      dec_advance<C::TK>(a, UPB, cur);  // the piece ended at the unit's last tile
+      load_q(cur, qa);
+    }
+    // Each warp leaves (m, l, u) of its rows; one barrier; each thread merges
+    // GC*D / THREADS output elements over the warps.
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+    if (row_live) {
+      if (t4 == 0) {
+        wm_sm[warp * GC + g] = m_run;
+        wl_sm[warp * GC + g] = l_part;
+      }
+      float* sl = sl_sm + (warp * GC + g) * D + 2 * t4;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) *reinterpret_cast<float2*>(sl + 8 * n) = make_float2(o[n][0], o[n][1]);
+    }
+    __syncthreads();
+    const bool live = !*abort_flag;
+    const size_t pslot = (size_t)u_idx * a.slots + slot;
     for (int i = tid; i < GC * D; i += C::THREADS) {
-      const int g = i / D;
-      float u = 0.f;
+      const int gi = i / D, col = i % D;
+      float M = -CUDART_INF_F;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) u += red[(w * GC + g) * D + i % D];
-      a.o[(size_t)(b * a.Hq + h0 + g) * D + i % D] = __float2bfloat16_rn(u / l_s[g]);
-    }
-    if (a.lse != nullptr && tid < GC)
-      a.lse[b * a.Hq + h0 + tid] = (m_s[tid] + log2f(l_s[tid])) * 0.69314718055994531f;
-    return;
-  }
-  // Partial of this split: normalised o and its base-2 lse.
-  for (int i = tid; i < GC * D; i += C::THREADS) {
-    const int g = i / D;
-    float u = 0.f;
+      for (int w = 0; w < C::NW; ++w) M = fmaxf(M, wm_sm[w * GC + gi]);
+      const float mr = (M == -CUDART_INF_F) ? 0.f : M;
+      float Lt = 0.f, val = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) u += red[(w * GC + g) * D + i % D];
-    a.part_o[((pbase + split_idx) * GC + g) * D + i % D] = u / l_s[g];
-  }
-  if (tid < GC) a.part_lse[(pbase + split_idx) * GC + tid] = m_s[tid] + log2f(l_s[tid]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int ticket = atomicAdd(a.tickets + unit, 1);
-    *flag_s = (ticket == n_splits - 1) ? 2 : 0;
-  }
-  __syncthreads();
-  if (*flag_s != 2) return;
-  // Last split to finish: merge all partials of this unit.
-  __threadfence();
-  if (tid < GC) {
-    float mx = -CUDART_INF_F;
-    for (int sp = 0; sp < n_splits; ++sp)
-      mx = fmaxf(mx, __ldcg(a.part_lse + (pbase + sp) * GC + tid));
-    float tot = 0.f;
-    for (int sp = 0; sp < n_splits; ++sp) {
-      const float w = ex2_approx(__ldcg(a.part_lse + (pbase + sp) * GC + tid) - mx);
-      tot += w;
+      for (int w = 0; w < C::NW; ++w) {
+        const float f = ex2_approx(wm_sm[w * GC + gi] - mr);
+        Lt = fmaf(wl_sm[w * GC + gi], f, Lt);
+        val = fmaf(sl_sm[(w * GC + gi) * D + col], f, val);
+      }
+      if (!live) continue;
+      const float ov = Lt > 0.f ? val / Lt : 0.f;
+      const float lse2 = Lt > 0.f ? M + log2f(Lt) : -CUDART_INF_F;  // base 2
+      if (whole) {
+        a.o[((size_t)b * a.Hq + h0 + gi) * D + col] = __float2bfloat16_rn(ov);
+        if (a.lse != nullptr && col == 0)
+          a.lse[(size_t)b * a.Hq + h0 + gi] = lse2 * 0.69314718055994531f;
+      } else {
+        a.part_o[pslot * GC * D + i] = ov;
+        if (col == 0) a.part_lse[pslot * GC + gi] = lse2;
+      }
     }
-    m_s[tid] = mx;
-    l_s[tid] = tot;
-    if (a.lse != nullptr) a.lse[b * a.Hq + h0 + tid] = (mx + log2f(tot)) * 0.69314718055994531f;
-  }
-  __syncthreads();
-  for (int i = tid; i < GC * D; i += C::THREADS) {
-    const int g = i / D;
-    float u = 0.f;
-    for (int sp = 0; sp < n_splits; ++sp) {
-      const float w = ex2_approx(__ldcg(a.part_lse + (pbase + sp) * GC + g) - m_s[g]);
-      u = fmaf(w, __ldcg(a.part_o + ((pbase + sp) * GC + g) * D + i % D), u);
+    if (!whole) {
+      pend_u[pend_n] = u_idx;
+      pend_pieces[pend_n] = pieces;
+      pend_b[pend_n] = b;
+      pend_h0[pend_n] = h0;
+      ++pend_n;
     }
-    a.o[(size_t)(b * a.Hq + h0 + g) * D + i % D] = __float2bfloat16_rn(u / l_s[g]);
+    __syncthreads();  // the slices are free again
   }
-  if (tid == 0) a.tickets[unit] = 0;  // ready for the next call
+
+  // ---- settle the partial pieces: the last piece of a unit to finish merges.
+  if (pend_n > 0) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const bool live = !*abort_flag;
+      for (int k = 0; k < pend_n; ++k)
+        last_flag[k] = live ? (atomicAdd(a.tickets + pend_u[k], 1) == pend_pieces[k] - 1) : 0;
+    }
+    __syncthreads();
+    for (int k = 0; k < pend_n; ++k) {
+      if (!last_flag[k]) continue;
+      __threadfence();
+      const int pieces = pend_pieces[k];
+      const float* plse = a.part_lse + (size_t)pend_u[k] * a.slots * GC;
+      const float* po = a.part_o + (size_t)pend_u[k] * a.slots * GC * D;
+      for (int i = tid; i < GC * D; i += C::THREADS) {
+        const int gi = i / D;
+        float mx = -CUDART_INF_F;
+        for (int sp = 0; sp < pieces; ++sp) mx = fmaxf(mx, __ldcg(plse + sp * GC + gi));
+        const float mr = (mx == -CUDART_INF_F) ? 0.f : mx;
+        float tot = 0.f, u = 0.f;
+        for (int sp = 0; sp < pieces; ++sp) {
+          const float wgt = ex2_approx(__ldcg(plse + sp * GC + gi) - mr);
+          tot += wgt;
+          u = fmaf(wgt, __ldcg(po + (size_t)sp * GC * D + i), u);
+        }
+        a.o[((size_t)pend_b[k] * a.Hq + pend_h0[k] + gi) * D + (i % D)] =
+            __float2bfloat16_rn(tot > 0.f ? u / tot : 0.f);
+        if (a.lse != nullptr && (i % D) == 0)
+          a.lse[(size_t)pend_b[k] * a.Hq + pend_h0[k] + gi] =
+              tot > 0.f ? (mx + log2f(tot)) * 0.69314718055994531f : -CUDART_INF_F;
+      }
+      if (tid == 0) a.tickets[pend_u[k]] = 0;  // ready for the next call
+    }
+  }
+
+  // Copies still in flight (only after a wait gave up) land before the CTA exits.
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    for (int s = 0; s < C::STAGES; ++s)
+      if (fills[s] > 0) mbar_wait(full + s, (fills[s] - 1) & 1, a.status, kSiteDecDrain);
+  }
 }
 
 }  // namespace attn_dev

@@ -104,7 +104,7 @@ def _dec(lib, q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hk
     (dict(kc=FAKE + 4), binding.ERR_INVALID_ARG),
     (dict(scale=0.0), binding.ERR_INVALID_ARG),
     (dict(d=80), binding.ERR_UNSUPPORTED),
-    (dict(B=40000, Hkv=2), binding.ERR_UNSUPPORTED),  # too many (sequence, head) units for one grid
+    (dict(B=1 << 20, Hq=32, Hkv=32), binding.ERR_UNSUPPORTED),  # more (sequence, head) units than 2^24
 ])
 def test_decode_argument_checks(lib, kw, code):
     assert _dec(lib, **kw) == code

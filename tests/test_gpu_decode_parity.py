@@ -76,3 +76,22 @@ def test_decode_workspace_reuse_and_status():
     o_ref3, lse_ref3 = oracle.attention_decode(f64(q), f64(kc), f64(vc), clamped.numpy(), w.scale)
     compare(o3, l3, o_ref3, lse_ref3, "clamped")
     assert binding.device_status()[0] == binding.OK   # cleared by the read
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,d,lens", [
+    # one long sequence: its tiles are spread over many CTAs and merged by the last one
+    (1, 8, 1, 20000, 128, [20000]),
+    (2, 4, 2, 9000, 64, [9000, 8999]),
+    # many short sequences: each CTA's chunk spans many whole units
+    (300, 16, 4, 260, 128, None),
+    (64, 32, 8, 1500, 128, None),
+], ids=["long_mqa", "long_d64", "many_short", "gqa_b64"])
+def test_decode_balanced_partition(B, Hq, Hkv, Lmax, d, lens):
+    w = Decode("partition", B=B, Hq=Hq, Hkv=Hkv, Lmax=Lmax, Lmin=0, d=d, seed=34)
+    q, kc, vc, sl = decode_inputs(w)
+    if lens is not None:
+        sl = torch.tensor(lens, dtype=torch.int32)
+    o, lse = _run(q, kc, vc, sl, w.scale)
+    o_ref, lse_ref = oracle.attention_decode(f64(q), f64(kc), f64(vc), sl.numpy(), w.scale)
+    compare(o, lse, o_ref, lse_ref, f"partition B={B} Lmax={Lmax}")
+    assert binding.device_status()[0] == binding.OK
