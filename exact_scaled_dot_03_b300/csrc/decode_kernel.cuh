@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
   // Partial pieces of this CTA (its first and/or last), settled after the stream.
   int pend_n = 0;
   int pend_u[2], pend_pieces[2], pend_b[2], pend_h0[2];
+  bool pend_early[2] = {false, false};  // ticket already taken (a first piece that was not the last)
+  bool pend_last[2] = {false, false};   // thread 0: the result of that early ticket
 
   int it_tile = 0;  // tiles of this CTA consumed so far (ring position)
   while (it_tile < n_tiles) {
@@ -462,24 +464,33 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
         if (col == 0) a.part_lse[pslot * GC + gi] = lse2;
       }
     }
+    __syncthreads();  // the slices are free again
     if (!whole) {
       pend_u[pend_n] = u_idx;
       pend_pieces[pend_n] = pieces;
       pend_b[pend_n] = b;
       pend_h0[pend_n] = h0;
+      // A first piece that is not also the last: thread 0 takes its ticket now
+      // (its fence then overlaps the stream); the other pieces of that unit were
+      // started by the previous CTA, so it is rarely the last to arrive.
+      pend_early[pend_n] = it_tile < n_tiles;
+      if (pend_early[pend_n] && tid == 0) {
+        __threadfence();
+        pend_last[pend_n] = live && atomicAdd(a.tickets + u_idx, 1) == pieces - 1;
+      }
       ++pend_n;
     }
-    __syncthreads();  // the slices are free again
   }
 
   // ---- settle the partial pieces: the last piece of a unit to finish merges.
   if (pend_n > 0) {
-    __threadfence();
-    __syncthreads();
+    __syncthreads();  // every thread's partial writes precede thread 0's fence
     if (tid == 0) {
       const bool live = !*abort_flag;
+      __threadfence();
       for (int k = 0; k < pend_n; ++k)
-        last_flag[k] = live ? (atomicAdd(a.tickets + pend_u[k], 1) == pend_pieces[k] - 1) : 0;
+        last_flag[k] = pend_early[k] ? pend_last[k]
+                                     : live && atomicAdd(a.tickets + pend_u[k], 1) == pend_pieces[k] - 1;
     }
     __syncthreads();
     for (int k = 0; k < pend_n; ++k) {
@@ -490,11 +501,24 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
       const float* po = a.part_o + (size_t)pend_u[k] * a.slots * GC * D;
       for (int i = tid; i < GC * D; i += C::THREADS) {
         const int gi = i / D;
-        float mx = -CUDART_INF_F;
-        for (int sp = 0; sp < pieces; ++sp) mx = fmaxf(mx, __ldcg(plse + sp * GC + gi));
+        // Up to 4 partials are loaded together (independent loads), more in a loop.
+        float ls[4], os[4];
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+          ls[sp] = sp < pieces ? __ldcg(plse + sp * GC + gi) : -CUDART_INF_F;
+          os[sp] = sp < pieces ? __ldcg(po + (size_t)sp * GC * D + i) : 0.f;
+        }
+        float mx = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
+        for (int sp = 4; sp < pieces; ++sp) mx = fmaxf(mx, __ldcg(plse + sp * GC + gi));
         const float mr = (mx == -CUDART_INF_F) ? 0.f : mx;
         float tot = 0.f, u = 0.f;
-        for (int sp = 0; sp < pieces; ++sp) {
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+          const float wgt = ex2_approx(ls[sp] - mr);
+          tot += wgt;
+          u = fmaf(wgt, os[sp], u);
+        }
+        for (int sp = 4; sp < pieces; ++sp) {
           const float wgt = ex2_approx(__ldcg(plse + sp * GC + gi) - mr);
           tot += wgt;
           u = fmaf(wgt, __ldcg(po + (size_t)sp * GC * D + i), u);
