@@ -369,6 +369,7 @@ def run_ours(args, w, wd):
             line["config"]["decode_workload"] = wd.name
         if do_pre:
             line["prefill_ms"] = tot["prefill"] / args.steps
+        line["per_step_ms"] = {name: [round(x, 4) for x in v] for name, v in ms.items()}
         if do_pre and do_dec:
             line["decode"] = dec_block
         line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,

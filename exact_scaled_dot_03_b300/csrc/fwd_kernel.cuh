@@ -280,14 +280,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = (c > rel) ? -CUDART_INF_F : sv[c];
       }
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+      // Row max with three-input max (half the instructions of a pairwise
+      // chain; four independent chains for latency).
+      float mx0 = fmax3(sv[0], sv[1], sv[2]), mx1 = fmax3(sv[3], sv[4], sv[5]);
+      float mx2 = fmax3(sv[6], sv[7], sv[8]), mx3 = fmax3(sv[9], sv[10], sv[11]);
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, sv[c]);
-        mx1 = fmaxf(mx1, sv[c + 1]);
-        mx2 = fmaxf(mx2, sv[c + 2]);
-        mx3 = fmaxf(mx3, sv[c + 3]);
+      for (int c = 12; c + 8 <= 128; c += 8) {
+        mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+        mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+        mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+        mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
       }
+      mx0 = fmax3(mx0, sv[124], sv[125]);
+      mx1 = fmax3(mx1, sv[126], sv[127]);
       const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const bool need = m_new > m_used + 8.0f;
       float alpha = 1.f;
@@ -306,10 +311,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c = 64 * half + 2 * i;
-          const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_ref));
-          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_ref));
-          l0 += p0;
-          l1 += p1;
+          float x0, x1;
+          fma2(x0, x1, sv[c], sv[c + 1], sl2, sl2, -m_ref, -m_ref);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          add2(l0, l1, p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + 32 * half, pk);
