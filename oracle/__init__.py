@@ -33,6 +33,7 @@ from .attention import (  # noqa: F401
     bf16_bits_to_f64,
     attention_forward,
     attention_decode,
+    attention_decode_paged,
     online_attention_rows,
     merge_two_blocks,
     score_bytes,

@@ -122,6 +122,50 @@ def attention_decode(q, k_cache, v_cache, seqlens, scale: float):
     return o, lse
 
 
+def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale: float, k_new=None, v_new=None):
+    """Decode step over a paged KV cache, with the new token's K/V appended first.
+
+    The KV cache is cut into fixed-size blocks ("pages") that are allocated on
+    demand and need not be contiguous; a per-sequence block table maps the
+    logical page number to the physical page ([IMR], section "FlashAttention 和
+    PagedAttention 不是同一种答案"; [PW] §3.3).
+
+    k_pages, v_pages: [num_pages, Hkv, page_size, d]; token position p of
+    sequence b lives in physical page block_table[b][p // page_size], row
+    p % page_size. seqlens[b] is the number of tokens already cached.
+    If k_new / v_new ([B, Hkv, d]) are given, they are first written at
+    position seqlens[b] (the caller has reserved that page) and the query
+    attends to positions 0..seqlens[b]; otherwise to 0..seqlens[b]-1.
+
+    Written as: apply the append to copies of the pages, gather each
+    sequence's positions page by page into a contiguous cache, then take the
+    plain decode definition (attention_decode). Returns (o, lse, k_pages_after,
+    v_pages_after).
+    """
+    kp = np.array(k_pages, dtype=np.float64, copy=True)
+    vp = np.array(v_pages, dtype=np.float64, copy=True)
+    num_pages, Hkv, page_size, d = kp.shape
+    B = len(seqlens)
+    lens = [int(x) for x in seqlens]
+    if k_new is not None:
+        for b in range(B):
+            pos = lens[b]
+            page = int(block_table[b][pos // page_size])
+            kp[page, :, pos % page_size] = np.asarray(k_new[b], np.float64)
+            vp[page, :, pos % page_size] = np.asarray(v_new[b], np.float64)
+        lens = [x + 1 for x in lens]
+    Lmax = max(1, max(lens))
+    kc = np.zeros((B, Hkv, Lmax, d))
+    vc = np.zeros((B, Hkv, Lmax, vp.shape[-1]))
+    for b in range(B):
+        for pos in range(lens[b]):
+            page = int(block_table[b][pos // page_size])
+            kc[b, :, pos] = kp[page, :, pos % page_size]
+            vc[b, :, pos] = vp[page, :, pos % page_size]
+    o, lse = attention_decode(q, kc, vc, np.array(lens), scale)
+    return o, lse, kp, vp
+
+
 def online_attention_rows(q, k, v, scale: float, tile: int, causal_offset=None):
     """The blockwise recurrence of [AUT] §8 (its first two equations), literally.
 

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 from oracle import (
+    attention_decode_paged,
     attention_decode,
     attention_forward,
     bf16_bits_to_f64,
@@ -370,3 +371,79 @@ def test_decode_matches_prefix_attention_and_sdpa():
     assert (o0[:2] == 0).all() and np.isneginf(l0[:2]).all()
     with pytest.raises(ValueError):
         attention_decode(q, kc, vc, np.array([1, 41, 2]), scale)
+
+
+# --- paged decode with the new token appended -----------------------------------------------
+
+def _sdpa_decode(q_b, keys, vals, scale, G):
+    """torch SDPA (fp64) for one sequence: q_b [Hq, d], keys/vals [Hkv, L, d]."""
+    tq = torch.from_numpy(q_b[:, None, :])
+    tk = torch.from_numpy(keys).repeat_interleave(G, dim=0)
+    tv = torch.from_numpy(vals).repeat_interleave(G, dim=0)
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)[:, 0].numpy()
+    lse = torch.logsumexp(torch.einsum("hd,hjd->hj", tq[:, 0], tk) * scale, -1).numpy()
+    return o, lse
+
+
+@pytest.mark.parametrize("page_size", [4, 8, 16])
+def test_paged_decode_gathers_pages_through_the_block_table(page_size):
+    """Blocks of the KV cache need not be contiguous ([IMR] PagedAttention section;
+    [PW] §3.3): position p of sequence b is row p % P of physical page
+    block_table[b][p // P]. Checked against SDPA on keys gathered by that rule,
+    with a shuffled page pool; permuting the physical pages (and the table) changes nothing."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, d, num_pages = 3, 8, 2, 16, 24
+    seqlens = np.array([1, page_size * 2, page_size * 3 + 1])
+    kp, vp = _rand(rng, num_pages, Hkv, page_size, d), _rand(rng, num_pages, Hkv, page_size, d)
+    perm = rng.permutation(num_pages)
+    bt = perm[: B * 6].reshape(B, 6)
+    q = _rand(rng, B, Hq, d)
+    scale = 1 / math.sqrt(d)
+    o, lse, kp2, vp2 = attention_decode_paged(q, kp, vp, bt, seqlens, scale)
+    np.testing.assert_array_equal(kp2, kp)  # no append: pages untouched
+    for b in range(B):
+        L = seqlens[b]
+        keys = np.stack([kp[bt[b][p // page_size], :, p % page_size] for p in range(L)], axis=1)
+        vals = np.stack([vp[bt[b][p // page_size], :, p % page_size] for p in range(L)], axis=1)
+        ro, rl = _sdpa_decode(q[b], keys, vals, scale, Hq // Hkv)
+        np.testing.assert_allclose(o[b], ro, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl, atol=1e-12)
+    # relabel physical pages: same attention
+    relabel = rng.permutation(num_pages)
+    kp3, vp3 = np.empty_like(kp), np.empty_like(vp)
+    kp3[relabel], vp3[relabel] = kp, vp
+    o3, lse3, _, _ = attention_decode_paged(q, kp3, vp3, relabel[bt], seqlens, scale)
+    np.testing.assert_allclose(o3, o, atol=1e-15)
+    np.testing.assert_allclose(lse3, lse, atol=1e-15)
+
+
+def test_paged_decode_appends_the_new_token_before_attending():
+    """The new token's K/V is written at position seqlens[b] and attended to
+    together with the cache ([PW] §3.1: the new token's K/V joins the cache)."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, d, P, num_pages = 4, 4, 1, 8, 4, 16
+    seqlens = np.array([0, 3, 4, 7])  # 4: the append opens a new page
+    kp, vp = _rand(rng, num_pages, Hkv, P, d), _rand(rng, num_pages, Hkv, P, d)
+    bt = rng.permutation(num_pages)[: B * 3].reshape(B, 3)
+    q, kn, vn = _rand(rng, B, Hq, d), _rand(rng, B, Hkv, d), _rand(rng, B, Hkv, d)
+    scale = 0.7
+    o, lse, kp2, vp2 = attention_decode_paged(q, kp, vp, bt, seqlens, scale, kn, vn)
+    for b in range(B):
+        L = seqlens[b]
+        pg, row = bt[b][L // P], L % P
+        np.testing.assert_array_equal(kp2[pg, :, row], kn[b])
+        np.testing.assert_array_equal(vp2[pg, :, row], vn[b])
+        gather = lambda pages: (np.stack([pages[bt[b][p // P], :, p % P] for p in range(L)], axis=1) if L
+                                else np.zeros((Hkv, 0, d)))
+        keys = np.concatenate([gather(kp), kn[b][:, None]], axis=1)
+        vals = np.concatenate([gather(vp), vn[b][:, None]], axis=1)
+        ro, rl = _sdpa_decode(q[b], keys, vals, scale, Hq // Hkv)
+        np.testing.assert_allclose(o[b], ro, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl, atol=1e-12)
+    # a cache of length 0 plus the appended token: the output is that token's value
+    np.testing.assert_allclose(o[0], np.repeat(vn[0], Hq // Hkv, axis=0), atol=1e-15)
+    # every other page row is left as it was
+    changed = np.zeros(kp.shape[:1] + kp.shape[2:3], bool)
+    for b in range(B):
+        changed[bt[b][seqlens[b] // P], seqlens[b] % P] = True
+    np.testing.assert_array_equal(kp2[~changed[:, None, :].repeat(Hkv, 1)], kp[~changed[:, None, :].repeat(Hkv, 1)])
