@@ -5,8 +5,9 @@
 
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
 already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
-N=16384, d=128) followed by a decode step (B=16, Hq=32, Hkv=8, d=128, cache
-lengths uniform on [1024, 8192]). L2 is flushed (a 256 MiB write) before each
+N=16384, d=128), a decode step (B=16, Hq=32, Hkv=8, d=128, cache lengths
+uniform on [1024, 8192]) and the same decode over a paged cache (64-token
+pages) with the new token appended. L2 is flushed (a 256 MiB write) before each
 of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
 read so the timed kernel does not pay for writing back the flush's dirty lines.
 Prints one JSON line.
@@ -246,6 +247,7 @@ def run_ours(args, w, wd):
     stream = torch.cuda.current_stream()
     do_pre = args.only in (None, "prefill")
     do_dec = args.only in (None, "decode")
+    do_pag = args.only in (None, "paged")
 
     parts = []  # (name, launch function)
     if do_pre:
@@ -262,6 +264,19 @@ def run_ours(args, w, wd):
         ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
         parts.append(("decode", lambda: binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do,
                                                        lse=dlse)))
+    if do_pag:
+        wp = W.DECODE_GQA_PAGED
+        pq_h, pkn_h, pvn_h, pkp_h, pvp_h, pbt_h, psl_h = W.paged_decode_inputs(wp)
+        pq, pkn, pvn, pkp, pvp, pbt, psl = (t.to(dev) for t in (pq_h, pkn_h, pvn_h, pkp_h, pvp_h, pbt_h, psl_h))
+        po = torch.empty_like(pq)
+        plse = torch.empty(wp.B, wp.Hq, dtype=torch.float32, device=dev)
+        pws = torch.zeros(int(binding.lib().attn_decode_paged_workspace_size(wp.B, wp.Hq, wp.Hkv, pbt.shape[1],
+                                                                             wp.page_size, wp.d)),
+                          dtype=torch.uint8, device=dev)
+        # Every call appends at position seqlens[b] (the same slot each time: the
+        # lengths are not advanced between timed calls, so the work is identical).
+        parts.append(("paged", lambda: binding.decode_paged(pq, pkp, pvp, pbt, psl, pkn, pvn, scale=wp.scale,
+                                                            workspace=pws, out=po, lse=plse)))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     clean_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -345,6 +360,21 @@ def run_ours(args, w, wd):
                      "ms": tot["decode"] / args.steps, "roofline": dec_roof}
         if not do_pre:   # decode alone: its numbers are the line's
             value, unit, roofline = dec_value, "GB/s", dec_roof
+    pag_block = None
+    if do_pag:
+        pag_bytes = ((int(psl_h.sum()) + wp.B) * wp.Hkv * wp.d * 2 * 2 + 2 * wp.B * wp.Hq * wp.d * 2
+                     + 4 * wp.B * wp.Hq + 2 * wp.B * wp.Hkv * wp.d * 2 * 2)
+        pag_value = world * pag_bytes * args.steps / (tot["paged"] / 1e3) / 1e9
+        pag_achieved = pag_bytes / (statistics.mean(ms["paged"]) / 1e3) / 1e9
+        pag_roof = {"bound": "hbm", "achieved": pag_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": pag_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
+                    "traffic": None, "algorithmic_bytes_per_launch": pag_bytes,
+                    "kernel": "attn_decode_kernel<128,4> (paged, append)"}
+        pag_block = {"metric": "paged decode + append GB/s (cache rows read incl. the new token, q/o/lse, "
+                               "appended rows read and written)", "workload": wp.name, "value": pag_value,
+                     "unit": "GB/s", "ms": tot["paged"] / args.steps, "roofline": pag_roof}
+        if not do_pre and not do_dec:
+            value, unit, roofline = pag_value, "GB/s", pag_roof
 
     e2e = None
     if do_pre and not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
@@ -361,7 +391,7 @@ def run_ours(args, w, wd):
             "warmup": args.warmup, "ms_per_step": sum(tot.values()) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16)",
-            "config": {"workload": w.name if do_pre else wd.name,
+            "config": {"workload": w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name,
                        "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         }
@@ -372,6 +402,8 @@ def run_ours(args, w, wd):
         line["per_step_ms"] = {name: [round(x, 4) for x in v] for name, v in ms.items()}
         if do_pre and do_dec:
             line["decode"] = dec_block
+        if pag_block is not None and (do_pre or do_dec):
+            line["decode_paged"] = pag_block
         line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
                      "clocks": clocks, "wall_s_timed_region": t_wall})
         print(json.dumps(line), flush=True)
@@ -424,7 +456,7 @@ def main():
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged"], default=None,
                     help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -31,6 +31,9 @@ SIGNATURES = {
     "attn_kv_cache_bytes": (_u64, [_i64, _i64, _i64, _i64, _i]),
     "attn_version": (ctypes.c_char_p, []),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "attn_decode_paged_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "attn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                               _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -150,6 +153,47 @@ def decode(q, k_cache, v_cache, seqlens, scale: float | None = None, workspace=N
                              B, Hq, Hkv, Lmax, d, s, workspace.data_ptr(), workspace.numel(),
                              _stream_handle(stream))
     _check(code, "attn_decode")
+    return o, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, k_new=None, v_new=None, scale: float | None = None,
+                 workspace=None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Paged KV-cache decode with optional fused append: returns (o, lse); see
+    ``attn_decode_paged`` in include/attn.h.
+
+    q: [B, Hq, d]; pages: [num_pages, Hkv, page_size, d] bf16; block_table:
+    [B, max_pages] int32; seqlens: [B] int32 (tokens already cached); k_new,
+    v_new: [B, Hkv, d] bf16 or None. The appended rows are written into the pages.
+    """
+    _need(q, "q", dims=3)
+    _need(k_pages, "k_pages", dims=4)
+    _need(v_pages, "v_pages", dims=4)
+    _need(block_table, "block_table", dtype=torch.int32, dims=2)
+    _need(seqlens, "seqlens", dtype=torch.int32, dims=1)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _need(k_new, "k_new", dims=3)
+        _need(v_new, "v_new", dims=3)
+    B, Hq, d = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if workspace is None:
+        n = int(lib().attn_decode_paged_workspace_size(B, Hq, Hkv, max_pages, page_size, d))
+        if n == 0:
+            raise AttnError(ERR_UNSUPPORTED, "attn_decode_paged_workspace_size")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", dtype=torch.uint8, dims=1)
+    o = torch.empty_like(q) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    s = default_scale(d) if scale is None else float(scale)
+    code = lib().attn_decode_paged(q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
+                                   v_new.data_ptr() if v_new is not None else None, k_pages.data_ptr(),
+                                   v_pages.data_ptr(), block_table.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, B, Hq, Hkv, num_pages, page_size,
+                                   max_pages, d, s, workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(code, "attn_decode_paged")
     return o, lse
 
 

@@ -162,16 +162,32 @@ int sm_count(int dev) {
   return counts[dev];
 }
 
+// Paged-cache layout and fused append for a decode launch (all null/zero for
+// a contiguous cache without append).
+struct DecodePaging {
+  const int32_t* block_table = nullptr;
+  int bt_stride = 0, page_size = 0, num_pages = 0;
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+};
+
 template <int D, int GC>
 attn_status launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seqlens, void* o,
                           float* lse, int B, int Hq, int Hkv, int Lmax, float scale, void* ws,
-                          const DecodePlan& plan, cudaStream_t stream, int dev) {
+                          const DecodePlan& plan, cudaStream_t stream, int dev, const DecodePaging& pg) {
   static bool smem_set[kMaxDevices] = {};
   using C = DecCfg<D, GC>;
   CUtensorMap tk, tv;
-  if (!make_map(&tk, kc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK) ||
-      !make_map(&tv, vc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK))
-    return ATTN_ERR_CUDA;
+  if (pg.block_table == nullptr) {
+    if (!make_map(&tk, kc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK) ||
+        !make_map(&tv, vc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK))
+      return ATTN_ERR_CUDA;
+  } else {
+    const int rows = pg.page_size < C::TK ? pg.page_size : C::TK;
+    if (!make_map(&tk, kc, D, pg.page_size, static_cast<long long>(pg.num_pages) * Hkv, rows) ||
+        !make_map(&tv, vc, D, pg.page_size, static_cast<long long>(pg.num_pages) * Hkv, rows))
+      return ATTN_ERR_CUDA;
+  }
   if (!ensure_smem(attn_decode_kernel<D, GC>, C::SMEM_BYTES, dev, smem_set)) return ATTN_ERR_CUDA;
   DecArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -192,6 +208,14 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = status_ptr(dev);
   if (a.status == nullptr) return ATTN_ERR_CUDA;
+  a.block_table = pg.block_table;
+  a.bt_stride = pg.bt_stride;
+  a.page_size = pg.page_size;
+  a.num_pages = pg.num_pages;
+  a.k_new = static_cast<const __nv_bfloat16*>(pg.k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(pg.v_new);
+  a.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(kc));
+  a.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(vc));
   static_assert(C::TK == kDecTile && C::MIN_CHUNK == kDecMinChunk, "decode plan and kernel disagree");
   const int grid = sm_count(dev);  // persistent: one CTA per SM
   if (grid == 0) return ATTN_ERR_CUDA;
@@ -202,12 +226,13 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
 template <int D>
 attn_status dispatch_decode_gc(const void* q, const void* kc, const void* vc, const int32_t* seqlens, void* o,
                                float* lse, int B, int Hq, int Hkv, int Lmax, float scale, void* ws,
-                               const DecodePlan& plan, cudaStream_t stream, int dev) {
+                               const DecodePlan& plan, cudaStream_t stream, int dev,
+                               const DecodePaging& pg = DecodePaging()) {
   switch (plan.GC) {
-    case 8: return launch_decode<D, 8>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
-    case 4: return launch_decode<D, 4>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
-    case 2: return launch_decode<D, 2>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
-    default: return launch_decode<D, 1>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev);
+    case 8: return launch_decode<D, 8>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev, pg);
+    case 4: return launch_decode<D, 4>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev, pg);
+    case 2: return launch_decode<D, 2>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev, pg);
+    default: return launch_decode<D, 1>(q, kc, vc, seqlens, o, lse, B, Hq, Hkv, Lmax, scale, ws, plan, stream, dev, pg);
   }
 }
 
@@ -271,6 +296,56 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
                                  dev);
 }
 
+namespace {
+bool valid_page_size(int p) { return p >= 8 && ((p % 128 == 0) || (128 % p == 0)) && p <= (1 << 20); }
+}  // namespace
+
+size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_pages_per_seq, int page_size, int d) {
+  if (max_pages_per_seq < 1 || !valid_page_size(page_size)) return 0;
+  const long long cap = static_cast<long long>(max_pages_per_seq) * page_size;
+  if (cap > (1LL << 30)) return 0;
+  DecodePlan p;
+  return plan_decode(B, Hq, Hkv, static_cast<int>(cap), d, &p) ? p.total : 0;
+}
+
+attn_status attn_decode_paged(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                              const int32_t* block_table, const int32_t* seqlens, void* o, float* lse, int B, int Hq,
+                              int Hkv, int num_pages, int page_size, int max_pages_per_seq, int d, float scale,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || block_table == nullptr || seqlens == nullptr ||
+      o == nullptr || workspace == nullptr || ((k_new == nullptr) != (v_new == nullptr)))
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || num_pages < 1 || max_pages_per_seq < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16) ||
+      !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(workspace, 16) || !aligned(block_table, 4) ||
+      !aligned(seqlens, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!valid_page_size(page_size)) return ATTN_ERR_UNSUPPORTED;
+  const long long cap = static_cast<long long>(max_pages_per_seq) * page_size;
+  if (cap > (1LL << 30) || static_cast<long long>(num_pages) * Hkv > (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  if (!plan_decode(B, Hq, Hkv, static_cast<int>(cap), d, &plan)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < plan.total) return ATTN_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  DecodePaging pg;
+  pg.block_table = block_table;
+  pg.bt_stride = max_pages_per_seq;
+  pg.page_size = page_size;
+  pg.num_pages = num_pages;
+  pg.k_new = k_new;
+  pg.v_new = v_new;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return dispatch_decode_gc<64>(q, k_pages, v_pages, seqlens, o, lse, B, Hq, Hkv, static_cast<int>(cap), scale,
+                                  workspace, plan, s, dev, pg);
+  return dispatch_decode_gc<128>(q, k_pages, v_pages, seqlens, o, lse, B, Hq, Hkv, static_cast<int>(cap), scale,
+                                 workspace, plan, s, dev, pg);
+}
+
 attn_status attn_device_status(void* stream, unsigned* detail) {
   const int dev = current_device();
   if (dev < 0) return ATTN_ERR_CUDA;
@@ -285,7 +360,7 @@ attn_status attn_device_status(void* stream, unsigned* detail) {
     detail[2] = words[2];
   }
   if (words[0] & kStatusWaitTimeout) return ATTN_ERR_TIMEOUT;
-  if (words[0] & kStatusBadSeqlen) return ATTN_ERR_DEVICE_ARG;
+  if (words[0] & (kStatusBadSeqlen | kStatusBadPage)) return ATTN_ERR_DEVICE_ARG;
   return ATTN_OK;
 }
 
@@ -296,7 +371,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
-    case ATTN_ERR_DEVICE_ARG: return "device saw a sequence length outside [0, Lmax]";
+    case ATTN_ERR_DEVICE_ARG: return "device saw a sequence length outside [0, Lmax] or a page id outside [0, num_pages)";
   }
   return "unknown status";
 }

@@ -64,6 +64,18 @@ struct DecArgs {
   int slots;               // partial slots per unit (>= pieces any unit can be cut into)
   float scale_log2;        // scale * log2(e)
   unsigned* status;
+  // Paged cache (block_table != nullptr): position p of sequence b is row
+  // p % page_size of page block_table[b * bt_stride + p / page_size] of the
+  // [num_pages, Hkv, page_size, D] cache; page_size divides 128 or is a
+  // multiple of it. Otherwise the cache is [B, Hkv, Lmax, D].
+  const int* block_table;
+  int bt_stride, page_size, num_pages;
+  // Fused append (k_new != nullptr): the new token's K/V [B, Hkv, D] is written
+  // at position seqlens[b] of the cache and attended to with the cached keys.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
 };
 
 template <int D, int GC>
@@ -103,10 +115,30 @@ struct TileCursor {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Cache length of sequence b, clamped into [0, Lmax].
+// Keys sequence b attends to: its cached length, clamped into
+// [0, Lmax - 1 if appending else Lmax], plus the appended token.
 __device__ __forceinline__ int dec_len(const DecArgs& a, int b) {
+  const int app = a.k_new != nullptr ? 1 : 0;
   const int L = a.seqlens[b];
-  return max(0, min(L, a.Lmax));
+  return max(0, min(L, a.Lmax - app)) + app;
+}
+
+// Physical page holding logical page lp of sequence b (flagged and replaced
+// by page 0 when the table holds an id outside [0, num_pages)).
+__device__ __forceinline__ int dec_page(const DecArgs& a, int b, int lp) {
+  const int pg = a.block_table[(size_t)b * a.bt_stride + lp];
+  if (pg < 0 || pg >= a.num_pages) {
+    atomicOr(a.status, kStatusBadPage);
+    return 0;
+  }
+  return pg;
+}
+
+// Element offset of the cache row holding position p of (sequence b, KV head hkv).
+__device__ __forceinline__ size_t dec_row_offset(const DecArgs& a, int b, int hkv, int p, int D) {
+  if (a.block_table == nullptr) return (((size_t)b * a.Hkv + hkv) * a.Lmax + p) * D;
+  const int pg = dec_page(a, b, p / a.page_size);
+  return (((size_t)pg * a.Hkv + hkv) * a.page_size + p % a.page_size) * D;
 }
 
 // Sum of x over the warp (all lanes receive it).
@@ -182,8 +214,8 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
       long long tiles = 0;
       if (b < a.B) {
         const int L = a.seqlens[b];
-        bad |= (L < 0 || L > a.Lmax);
-        tiles = (long long)((max(0, min(L, a.Lmax)) + C::TK - 1) / C::TK) * UPB;
+        bad |= (L < 0 || L > a.Lmax - (a.k_new != nullptr ? 1 : 0));
+        tiles = (long long)dec_tiles<C::TK>(a, b) * UPB;  // the same length rule as every walker below
       }
       total += warp_sum_ll(tiles);
     }
@@ -243,32 +275,59 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
   cur.j = static_cast<int>((t0 - cur.P) % cur.nt);
 
   // Loads tile `c` into stage s (one thread).
-  auto issue = [&](const TileCursor& c, int s) {
+  // Paged cache: a tile of TK keys is TK / rows page pieces (rows = min(page
+  // size, TK)); lane i < NSUB handles piece i. Its physical page is looked up
+  // one tile period before the copy is issued (see `ahead_pg`).
+  const int pg_rows = a.block_table != nullptr ? min(a.page_size, C::TK) : C::TK;
+  const int nsub = C::TK / pg_rows;
+  auto lookup_page = [&](const TileCursor& c) -> int {  // this lane's piece of tile c
+    if (a.block_table == nullptr || lane >= nsub) return 0;
+    const int last_lp = (dec_len(a, c.b) - 1) / a.page_size;  // pages past the length are not read
+    return dec_page(a, c.b, min((c.j * C::TK + lane * pg_rows) / a.page_size, last_lp));
+  };
+  // Loads tile c into stage s (warp-collective: lane 0 arms the barrier, the
+  // lanes of the page pieces issue their copies).
+  auto issue = [&](const TileCursor& c, int pg, int s) {
     uint8_t* kdst = ring + s * C::STAGE_BYTES;
     uint8_t* vdst = kdst + C::TILE_BYTES;
-    const int plane = c.b * a.Hkv + c.r / a.qgroups;
-    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+    const int hkv = c.r / a.qgroups;
+    if (lane == 0) mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+    __syncwarp();
+    if (a.block_table == nullptr) {
+      if (lane == 0) {
+        const int plane = c.b * a.Hkv + hkv;
 #pragma unroll
-    for (int kb = 0; kb < C::KBLK; ++kb) {
-      tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, c.j * C::TK, plane);
-      tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, c.j * C::TK, plane);
+        for (int kb = 0; kb < C::KBLK; ++kb) {
+          tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, c.j * C::TK, plane);
+          tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, c.j * C::TK, plane);
+        }
+      }
+    } else if (lane < nsub) {
+      const int plane = pg * a.Hkv + hkv;
+      const int row = (c.j * C::TK + lane * pg_rows) % a.page_size;
+#pragma unroll
+      for (int kb = 0; kb < C::KBLK; ++kb) {
+        tma_load_3d(kdst + kb * C::BOX_BYTES + lane * pg_rows * 128, &tm_k, full + s, kb * 64, row, plane);
+        tma_load_3d(vdst + kb * C::BOX_BYTES + lane * pg_rows * 128, &tm_v, full + s, kb * 64, row, plane);
+      }
     }
-    fills[s] += 1;
+    if (lane == 0) fills[s] += 1;
   };
 
-  // The first STAGES tiles are issued up front; after that, the last warp to
-  // release a stage refills it with the tile STAGES further on (`ahead`).
+  // The first STAGES tiles are issued up front by warp 0; after that, the last
+  // warp to release a stage refills it with the tile STAGES further on (`ahead`).
   TileCursor ahead = cur;
   for (int k = 0; k < C::STAGES && k < n_tiles; ++k) {
-    if (tid == 0) {
-      if (k == 0) {
+    if (warp == 0) {
+      if (k == 0 && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
       }
-      issue(ahead, k);
+      issue(ahead, lookup_page(ahead), k);
     }
     if (k + 1 < n_tiles) dec_advance<C::TK>(a, UPB, ahead);
   }
+  int ahead_pg = (C::STAGES < n_tiles) ? lookup_page(ahead) : 0;
 
   // Fragment coordinates (m16n8k16): lane = 4 g + t holds query row g and
   // key / value columns 2t, 2t+1 of each 8-wide n-tile.
@@ -326,6 +385,25 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
         const uint32_t vt = kt + C::TILE_BYTES;
         const int row0 = warp * C::KPW;          // first tile row of this warp
         const int key0 = jj * C::TK + row0;      // its key index in the sequence
+        if (a.k_new != nullptr && L - 1 >= key0 && L - 1 < key0 + C::KPW) {
+          // This warp's rows hold the appended token: put its K/V into the
+          // stage (whatever the cache row held when it was loaded), and have
+          // the first query group of the KV head store it in the cache.
+          const int hkv = cur.r / a.qgroups;
+          const int r = L - 1 - jj * C::TK;
+          const __nv_bfloat16* src = (lane < 16 ? a.k_new : a.v_new) + ((size_t)b * a.Hkv + hkv) * D;
+          uint8_t* stile = ring + s * C::STAGE_BYTES + (lane < 16 ? 0 : C::TILE_BYTES);
+          for (int c = lane & 15; c < D / 8; c += 16) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + 8 * c);
+            *reinterpret_cast<uint4*>(stile + (c >> 3) * C::BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = w;
+            if (cur.r % a.qgroups == 0) {
+              __nv_bfloat16* dst = (lane < 16 ? a.k_cache : a.v_cache) + dec_row_offset(a, b, hkv, L - 1, D);
+              *reinterpret_cast<uint4*>(dst + 8 * c) = w;
+            }
+          }
+          fence_proxy_async_smem();  // before a later TMA refill overwrites the stage
+          __syncwarp();
+        }
         // ---- S = Q K^T for this warp's 16 keys: n-tile 0 = keys 0-7, 1 = keys 8-15
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
@@ -400,16 +478,19 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
         }
       }
       __syncwarp();  // this warp's reads of the stage are done
+      int refill = 0;
       if (lane == 0) {
         __threadfence_block();
         const int done = atomicAdd(releases + s, 1) + 1;
-        if (done % C::NW == 0) {
-          // Last warp off this stage: refill it with the tile STAGES further on.
-          __threadfence_block();
-          if (it_tile + C::STAGES < n_tiles && !*abort_flag) issue(ahead, s);
-        }
+        // Last warp off this stage: it refills it with the tile STAGES further on.
+        refill = done % C::NW == 0 && it_tile + C::STAGES < n_tiles && !*abort_flag;
+        if (refill) __threadfence_block();
       }
-      if (it_tile + C::STAGES + 1 < n_tiles) dec_advance<C::TK>(a, UPB, ahead);
+      if (__shfl_sync(0xffffffffu, refill, 0)) issue(ahead, ahead_pg, s);
+      if (it_tile + C::STAGES + 1 < n_tiles) {
+        dec_advance<C::TK>(a, UPB, ahead);
+        ahead_pg = lookup_page(ahead);  // ready a tile period before it is needed
+      }
     }
 
     // ---- end of the piece. Start loading the next piece's queries first.

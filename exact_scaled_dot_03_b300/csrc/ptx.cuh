@@ -13,6 +13,7 @@ namespace attn_dev {
 enum : unsigned {
   kStatusWaitTimeout = 1u,   // a bounded mbarrier wait gave up
   kStatusBadSeqlen = 2u,     // a decode sequence length was outside [0, Lmax]
+  kStatusBadPage = 4u,       // a paged-decode block table held a page id outside [0, num_pages)
 };
 
 // A wait longer than this is a bug (no legitimate stage of these kernels takes

@@ -123,3 +123,68 @@ def bf16_bits(t: torch.Tensor):
     """Raw uint16 bit patterns of a bf16 tensor as a numpy array (no rounding)."""
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+@dataclass(frozen=True)
+class PagedDecode:
+    """One decode step over a paged KV cache, optionally appending the new token."""
+
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Lmin: int          # cached lengths uniform on [Lmin, Lmax] (before the append)
+    Lmax: int
+    d: int
+    page_size: int
+    append: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def max_pages(self) -> int:
+        return (self.Lmax + 1 + self.page_size - 1) // self.page_size  # room for the appended token
+
+    def with_(self, **kw) -> "PagedDecode":
+        return replace(self, **kw)
+
+
+def paged_decode_inputs(w: PagedDecode, lens=None):
+    """(q, k_new, v_new, k_pages, v_pages, block_table, seqlens), CPU tensors.
+
+    Draw order: cached lengths, q, k_new, v_new, the K page pool, the V page
+    pool, then a random permutation that hands out physical pages. Each
+    sequence gets the pages for its cached tokens plus the appended one; its
+    remaining block-table entries point at page 0. The pool has a few spare
+    pages so that not every page is in use.
+    """
+    gen = torch.Generator().manual_seed(w.seed)
+    seqlens = torch.randint(w.Lmin, w.Lmax + 1, (w.B,), generator=gen, dtype=torch.int64).to(torch.int32)
+    if lens is not None:
+        seqlens = torch.tensor(lens, dtype=torch.int32)
+    P = w.page_size
+    need = [(int(L) + 1 + P - 1) // P for L in seqlens]
+    num_pages = sum(need) + 3
+    q = _randn_bf16(gen, (w.B, w.Hq, w.d))
+    k_new = _randn_bf16(gen, (w.B, w.Hkv, w.d))
+    v_new = _randn_bf16(gen, (w.B, w.Hkv, w.d))
+    k_pages = _randn_bf16(gen, (num_pages, w.Hkv, P, w.d))
+    v_pages = _randn_bf16(gen, (num_pages, w.Hkv, P, w.d))
+    perm = torch.randperm(num_pages, generator=gen).to(torch.int32)
+    block_table = torch.zeros(w.B, w.max_pages, dtype=torch.int32)
+    nxt = 0
+    for b in range(w.B):
+        block_table[b, :need[b]] = perm[nxt:nxt + need[b]]
+        nxt += need[b]
+    if not w.append:
+        k_new = v_new = None
+    return q, k_new, v_new, k_pages, v_pages, block_table, seqlens
+
+
+# Paged form of the decode workload: the same shapes and length mix, 64-token
+# pages, the new token appended.
+DECODE_GQA_PAGED = PagedDecode("decode_paged_b16_hq32_hkv8_d128_l1024to8192_p64", B=16, Hq=32, Hkv=8, Lmin=1024,
+                               Lmax=8192, d=128, page_size=64, append=True, seed=1006)

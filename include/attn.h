@@ -59,7 +59,7 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128}) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
   ATTN_ERR_TIMEOUT = 4,     /* (device) an internal pipeline wait gave up */
-  ATTN_ERR_DEVICE_ARG = 5   /* (device) a decode sequence length was outside [0, Lmax] */
+  ATTN_ERR_DEVICE_ARG = 5   /* (device) a decode length outside [0, Lmax] or a page id outside [0, num_pages) */
 } attn_status;
 
 /*
@@ -113,6 +113,50 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int
 ATTN_API attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                         float* lse, int B, int Hq, int Hkv, int Lmax, int d, float scale, void* workspace,
                         size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes attn_decode_paged needs (0 for arguments it would reject).
+ * Same rules as attn_decode_workspace_size, with Lmax = max_pages_per_seq *
+ * page_size.
+ */
+ATTN_API size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_pages_per_seq, int page_size, int d);
+
+/*
+ * KV-cache decode over a paged cache, with the new token's K/V appended first.
+ *
+ * The cache is cut into fixed-size pages that are allocated on demand and need
+ * not be contiguous; a per-sequence block table maps logical page numbers to
+ * physical pages ([IMR] section "FlashAttention 和 PagedAttention 不是同一种
+ * 答案"; [PW] §3.3). The new token joins the cache before the query attends
+ * to it ([PW] §3.1).
+ *
+ *   q            [B, Hq, d] bf16 (device)
+ *   k_new, v_new [B, Hkv, d] bf16 (device), or both NULL (no append)
+ *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16 (device). Position p
+ *                of sequence b is row p % page_size of physical page
+ *                block_table[b * max_pages_per_seq + p / page_size].
+ *   block_table  [B, max_pages_per_seq] int32 (device); entries past a
+ *                sequence's last page are never read. An id outside
+ *                [0, num_pages) is flagged in the device status
+ *                (ATTN_ERR_DEVICE_ARG) and read as page 0.
+ *   seqlens      [B] int32 (device): tokens already cached. With an append the
+ *                new K/V is written at position seqlens[b] (the caller must
+ *                have mapped that position to a page) and the query attends to
+ *                positions 0..seqlens[b]; without one, to 0..seqlens[b]-1.
+ *                Lengths outside [0, capacity - (append ? 1 : 0)], capacity =
+ *                max_pages_per_seq * page_size, are clamped and flagged.
+ *   o, lse       as attn_decode.
+ *   page_size    a divisor of 128 that is >= 8, or a multiple of 128
+ *                (others: ATTN_ERR_UNSUPPORTED).
+ *   workspace    >= attn_decode_paged_workspace_size(...) bytes, zero-filled
+ *                before first use, left zero-filled by every completed call.
+ * The appended rows are the only cache memory written.
+ */
+ATTN_API attn_status attn_decode_paged(const void* q, const void* k_new, const void* v_new, void* k_pages,
+                                       void* v_pages, const int32_t* block_table, const int32_t* seqlens, void* o,
+                                       float* lse, int B, int Hq, int Hkv, int num_pages, int page_size,
+                                       int max_pages_per_seq, int d, float scale, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the calling thread's current

@@ -110,6 +110,38 @@ def test_decode_argument_checks(lib, kw, code):
     assert _dec(lib, **kw) == code
 
 
+def _paged(lib, q=FAKE, kn=FAKE, vn=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2,
+           num_pages=10, page_size=64, max_pages=4, d=128, scale=0.1, ws=FAKE, wsb=1 << 30):
+    return lib.attn_decode_paged(q, kn, vn, kp, vp, bt, sl, o, lse, B, Hq, Hkv, num_pages, page_size, max_pages, d,
+                                 scale, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=None), binding.ERR_INVALID_ARG),
+    (dict(kn=None), binding.ERR_INVALID_ARG),          # k_new without v_new
+    (dict(vn=None), binding.ERR_INVALID_ARG),
+    (dict(ws=None), binding.ERR_INVALID_ARG),
+    (dict(wsb=16), binding.ERR_INVALID_ARG),
+    (dict(num_pages=0), binding.ERR_INVALID_ARG),
+    (dict(max_pages=0), binding.ERR_INVALID_ARG),
+    (dict(bt=FAKE + 2), binding.ERR_INVALID_ARG),
+    (dict(kn=FAKE + 8), binding.ERR_INVALID_ARG),
+    (dict(page_size=48), binding.ERR_UNSUPPORTED),
+    (dict(page_size=4), binding.ERR_UNSUPPORTED),
+    (dict(page_size=192), binding.ERR_UNSUPPORTED),
+    (dict(d=96), binding.ERR_UNSUPPORTED),
+])
+def test_paged_decode_argument_checks(lib, kw, code):
+    assert _paged(lib, **kw) == code
+
+
+def test_paged_workspace_size(lib):
+    # same plan as the contiguous decode with Lmax = pages * page_size
+    assert binding.lib().attn_decode_paged_workspace_size(16, 32, 8, 128, 64, 128) == \
+        binding.decode_workspace_size(16, 32, 8, 8192, 128)
+    assert binding.lib().attn_decode_paged_workspace_size(16, 32, 8, 128, 48, 128) == 0
+
+
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     """Without the built library the binding raises; it never computes another way."""
     monkeypatch.setattr(binding, "_lib", None)
