@@ -55,7 +55,7 @@ def _two_pass_softmax(S: np.ndarray):
     return P, lse
 
 
-def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block: int = 1024):
+def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block: int = 1024, window: int = 0):
     """O = softmax(scale * Q K^T + mask) V per (batch, query head), and the LSE.
 
     q: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (float64). Returns o [B, Hq, R, d]
@@ -68,6 +68,11 @@ def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block:
     per row; O = P V. Rows are processed in blocks of ``row_block`` only to
     bound memory: each row's full score vector is materialised before its
     softmax, which is the same definition.
+
+    window > 0 adds a local window (Longformer-style local attention, [AUT]
+    §2 Longformer comparison; [PW] §6.1 sliding-window attention, O(n*w)):
+    query i, aligned with key i + (Nk - Nq), sees key j only if
+    |j - (i + Nk - Nq)| < window; with causal also j <= i + Nk - Nq.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -86,9 +91,11 @@ def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block:
             for r0 in range(0, rows.size, row_block):
                 ri = rows[r0:r0 + row_block]
                 S = scale * (q[b, h, ri] @ kh.T)
+                diag = ri[:, None] + (Nk - Nq)  # the key each query row is aligned with
                 if causal:
-                    hidden = keys[None, :] > (ri[:, None] + (Nk - Nq))
-                    S = np.where(hidden, -np.inf, S)
+                    S = np.where(keys[None, :] > diag, -np.inf, S)
+                if window > 0:
+                    S = np.where(np.abs(keys[None, :] - diag) >= window, -np.inf, S)
                 P, l = _two_pass_softmax(S)
                 o[b, h, r0:r0 + ri.size] = P @ vh
                 lse[b, h, r0:r0 + ri.size] = l

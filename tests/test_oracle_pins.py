@@ -447,3 +447,40 @@ def test_paged_decode_appends_the_new_token_before_attending():
     for b in range(B):
         changed[bt[b][seqlens[b] // P], seqlens[b] % P] = True
     np.testing.assert_array_equal(kp2[~changed[:, None, :].repeat(Hkv, 1)], kp[~changed[:, None, :].repeat(Hkv, 1)])
+
+
+# --- local (sliding-window) attention --------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("Nq,Nk,window", [(20, 20, 5), (12, 30, 7), (30, 12, 4), (16, 16, 1), (16, 16, 40)])
+def test_window_matches_sdpa_with_an_explicit_mask(causal, Nq, Nk, window):
+    """Local window ([AUT] §2 Longformer; [PW] §6.1): query i sees key j iff
+    |j - (i + Nk - Nq)| < w (and j <= i + Nk - Nq when causal). Checked
+    against torch SDPA with a boolean mask built from that rule."""
+    rng = np.random.default_rng(40 + window)
+    B, Hq, Hkv, d = 1, 4, 2, 8
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    o, lse = attention_forward(q, k, v, 0.5, causal, window=window)
+    i = np.arange(Nq)[:, None] + (Nk - Nq)
+    j = np.arange(Nk)[None, :]
+    allowed = np.abs(j - i) < window
+    if causal:
+        allowed &= j <= i
+    rows = allowed.any(axis=1)
+    tk = torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=1)
+    tv = torch.from_numpy(v).repeat_interleave(Hq // Hkv, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[:, :, rows]), tk, tv, attn_mask=torch.from_numpy(allowed[rows]), scale=0.5)
+    np.testing.assert_allclose(o[:, :, rows], ref.numpy(), atol=1e-12)
+    assert (o[:, :, ~rows] == 0).all() and np.isneginf(lse[:, :, ~rows]).all()
+    if window >= Nq + Nk:  # a window wider than everything is no window
+        o0, l0 = attention_forward(q, k, v, 0.5, causal)
+        np.testing.assert_array_equal(o, o0)
+
+
+def test_window_of_one_sees_only_the_aligned_key():
+    rng = np.random.default_rng(47)
+    q, k, v = _rand(rng, 1, 2, 10, 4), _rand(rng, 1, 2, 10, 4), _rand(rng, 1, 2, 10, 4)
+    o, lse = attention_forward(q, k, v, 1.0, True, window=1)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-15)
+    np.testing.assert_allclose(lse[0], np.einsum("hid,hid->hi", q[0], k[0]), atol=1e-12)
