@@ -23,6 +23,7 @@ _vp, _i, _f, _sz, _i64, _u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, c
                                 ctypes.c_int64, ctypes.c_uint64)
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "attn_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
@@ -91,8 +92,9 @@ def default_scale(d: int) -> float:
 
 
 def fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
-        stream=None):
-    """Exact attention forward: returns (o, lse); see ``attn_fwd`` in include/attn.h.
+        stream=None, window: int = 0):
+    """Exact attention forward: returns (o, lse); see ``attn_fwd`` / ``attn_fwd_window``
+    (window > 0: local window) in include/attn.h.
 
     q: [B, Hq, Nq, d], k/v: [B, Hkv, Nk, d], bf16 CUDA tensors.
     """
@@ -110,10 +112,10 @@ def fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, w
     if lse is not None:
         _need(lse, "lse", dtype=torch.float32, dims=3)
     s = default_scale(d) if scale is None else float(scale)
-    code = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                          lse.data_ptr() if lse is not None else None,
-                          B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)), _stream_handle(stream))
-    _check(code, "attn_fwd")
+    code = lib().attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None,
+                                 B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)), int(window), _stream_handle(stream))
+    _check(code, "attn_fwd_window")
     return o, lse
 
 

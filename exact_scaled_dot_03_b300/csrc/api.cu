@@ -92,7 +92,7 @@ __global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, size_t rows, int
 
 template <int D>
 attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, float scale, int causal, cudaStream_t stream, int dev) {
+                       int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream, int dev) {
   static bool smem_set[kMaxDevices] = {};
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -100,7 +100,10 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, flo
       !make_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, 128) ||
       !make_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, 128))
     return ATTN_ERR_CUDA;
-  if (!ensure_smem(attn_fwd_kernel<D>, C::SMEM_BYTES, dev, smem_set)) return ATTN_ERR_CUDA;
+  static bool smem_set_w[kMaxDevices] = {};
+  if (!ensure_smem(attn_fwd_kernel<D, false>, C::SMEM_BYTES, dev, smem_set) ||
+      !ensure_smem(attn_fwd_kernel<D, true>, C::SMEM_BYTES, dev, smem_set_w))
+    return ATTN_ERR_CUDA;
   FwdArgs a;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
@@ -112,12 +115,16 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.group = Hq / Hkv;
   a.causal = causal;
   a.causal_offset = Nk - Nq;
+  a.window = window;
   a.num_pairs = (Nq + 255) / 256;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = status_ptr(dev);
   if (a.status == nullptr) return ATTN_ERR_CUDA;
   dim3 grid(Hq, a.num_pairs, B);
-  attn_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+  if (window > 0)
+    attn_fwd_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+  else
+    attn_fwd_kernel<D, false><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -242,6 +249,12 @@ extern "C" {
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  return attn_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, 0, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int d, float scale, int causal, int window, void* stream) {
+  if (window < 0) return ATTN_ERR_INVALID_ARG;
   // k and v may be NULL only when there are no keys (an empty tensor has no storage).
   if (q == nullptr || o == nullptr || (Nk > 0 && (k == nullptr || v == nullptr))) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -262,8 +275,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     fill_empty_kernel<<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(o), lse, rows, d);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  if (d == 64) return launch_fwd<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, s, dev);
-  return launch_fwd<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, s, dev);
+  if (d == 64) return launch_fwd<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev);
+  return launch_fwd<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d) {

@@ -39,7 +39,8 @@ struct FwdArgs {
   int B, Hq, Hkv, Nq, Nk;
   int group;          // Hq / Hkv
   int causal;
-  int causal_offset;  // Nk - Nq: query i sees key j iff j <= i + causal_offset
+  int causal_offset;  // Nk - Nq: query i is aligned with key i + causal_offset
+  int window;         // > 0: query i sees key j only if |j - (i + causal_offset)| < window
   int num_pairs;      // ceil(Nq / 256)
   float scale_log2;   // scale * log2(e)
   unsigned* status;   // library status word (see kStatus*)
@@ -73,16 +74,40 @@ enum : unsigned {
   kSiteSFull, kSitePvDoneRescale, kSitePvDoneEpi, kSiteDrain, kSiteLoadDrain
 };
 
-// Number of 128-key tiles a 128-row query tile starting at row r0 must visit.
-__device__ __forceinline__ int fwd_num_kv_tiles(const FwdArgs& a, int r0) {
-  if (r0 >= a.Nq) return 0;
-  const int r_last = min(r0 + 127, a.Nq - 1);
-  const long long end = a.causal ? min((long long)a.Nk, (long long)r_last + a.causal_offset + 1)
-                                 : (long long)a.Nk;
-  return end <= 0 ? 0 : (int)((end + 127) / 128);
+// Keys query row r sees: [lo, hi] (empty if hi < lo). Causal: keys up to the
+// aligned one; local window: within window - 1 of it on either side
+// ([IMR] masking section; [AUT] §2 Longformer; [PW] §6.1).
+template <bool WIN>
+__device__ __forceinline__ void fwd_row_keys(const FwdArgs& a, long long r, int& lo, int& hi) {
+  const long long dg = r + a.causal_offset;
+  long long l = 0, h = (long long)a.Nk - 1;
+  if (WIN) {
+    l = max(l, dg - a.window + 1);
+    h = min(h, dg + a.window - 1);
+  }
+  if (a.causal) h = min(h, dg);
+  lo = (int)min(l, (long long)a.Nk);
+  hi = (int)max(h, -1LL);
 }
 
-template <int D>
+// The 128-key tiles [jb, je) a 128-row query tile starting at row r0 must
+// visit (both ends move forward with r0, so the rows' ranges are covered by
+// [lo(first row), hi(last row)]).
+template <bool WIN>
+__device__ __forceinline__ void fwd_kv_tiles(const FwdArgs& a, int r0, int& jb, int& je) {
+  jb = je = 0;
+  if (r0 >= a.Nq) return;
+  int lo, hi, lo2, hi2;
+  fwd_row_keys<WIN>(a, r0, lo, hi);
+  fwd_row_keys<WIN>(a, min(r0 + 127, a.Nq - 1), lo2, hi2);
+  if (hi2 < lo) return;
+  jb = WIN ? lo / 128 : 0;  // without a window every query tile starts at key 0
+  je = hi2 / 128 + 1;
+}
+
+// WIN: a local window is in force (the windowless instance keeps every range
+// offset a compile-time zero).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -112,10 +137,17 @@ __global__ void __launch_bounds__(320, 1)
   const int b = blockIdx.z;
   const int hkv = h / a.group;
   const int q_base = pair * 256;
-  int n_kv[2];
-  n_kv[0] = fwd_num_kv_tiles(a, q_base);
-  n_kv[1] = fwd_num_kv_tiles(a, q_base + 128);
-  const int n_kv_max = max(n_kv[0], n_kv[1]);
+  // Key tiles of query tile t: [jb[t], jb[t] + n_kv[t]); the CTA streams
+  // [j0, j0 + n_kv_max) of them, K/V stage = stream position % STAGES.
+  int jb[2], je[2], n_kv[2];
+  fwd_kv_tiles<WIN>(a, q_base, jb[0], je[0]);
+  fwd_kv_tiles<WIN>(a, q_base + 128, jb[1], je[1]);
+  n_kv[0] = je[0] - jb[0];
+  n_kv[1] = je[1] - jb[1];
+  const int j0 = !WIN ? 0 : n_kv[0] > 0 ? (n_kv[1] > 0 ? min(jb[0], jb[1]) : jb[0]) : jb[1];
+  const int n_kv_max = (n_kv[0] > 0 || n_kv[1] > 0)
+                           ? max(n_kv[0] > 0 ? je[0] : 0, n_kv[1] > 0 ? je[1] : 0) - j0 : 0;
+  auto uses = [&](int t, int j) { return j >= jb[t] && j < je[t]; };  // query tile t visits key tile j
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -159,9 +191,10 @@ __global__ void __launch_bounds__(320, 1)
                       b * a.Hq + h);
       }
       int issued = 0;
-      for (int j = 0; j < n_kv_max; ++j) {
-        const int s = j % C::STAGES;
-        const int u = j / C::STAGES;
+      for (int js = 0; js < n_kv_max; ++js) {
+        const int j = j0 + js;  // key tile
+        const int s = js % C::STAGES;
+        const int u = js / C::STAGES;
         if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, a.status, kSiteKEmpty)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(k_full + s, C::TILE_BYTES);
         for (int kb = 0; kb < C::KBLK; ++kb)
@@ -169,23 +202,23 @@ __global__ void __launch_bounds__(320, 1)
                       b * a.Hkv + hkv);
         if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, a.status, kSiteVEmpty)) {
           *abort_flag = 1;
-          issued = j + 1;  // K of tile j is in flight, V is not
+          issued = js + 1;  // K of this tile is in flight, V is not
           break;
         }
         mbar_arrive_expect_tx(v_full + s, C::TILE_BYTES);
         for (int kb = 0; kb < C::KBLK; ++kb)
           tma_load_3d(sV + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_v, v_full + s, kb * 64, j * 128,
                       b * a.Hkv + hkv);
-        issued = j + 1;
+        issued = js + 1;
         if (*abort_flag) break;
       }
       if (*abort_flag) {
         // Let every copy still in flight land before the CTA exits.
         mbar_wait(q_full, 0, a.status, kSiteLoadDrain);
-        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-          const int s = j % C::STAGES;
-          mbar_wait(k_full + s, (j / C::STAGES) & 1, a.status, kSiteLoadDrain);
-          mbar_wait(v_full + s, (j / C::STAGES) & 1, a.status, kSiteLoadDrain);
+        for (int js = max(0, issued - C::STAGES); js < issued; ++js) {
+          const int s = js % C::STAGES;
+          mbar_wait(k_full + s, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
+          mbar_wait(v_full + s, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
         }
       }
     }
@@ -195,16 +228,18 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       bool ok = mbar_wait(q_full, 0, a.status, kSiteQFull);
-      for (int j = 0; ok && j < n_kv_max; ++j) {
-        const int s = j % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1;
+      for (int js = 0; ok && js < n_kv_max; ++js) {
+        const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
+        const int s = js % C::STAGES;
+        const uint32_t ph = (js / C::STAGES) & 1;
         if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull))) break;
         tc_fence_after_sync();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_kv[t]) continue;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || !uses(t, j)) continue;
           // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
-          if (j > 0) {
-            if (!(ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneMma))) break;
+          if (j > jb[t]) {
+            if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma))) break;
             tc_fence_after_sync();
           }
           const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
@@ -221,16 +256,17 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(k_empty + s);
         if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull))) break;
         tc_fence_after_sync();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_kv[t]) continue;
-          if (!(ok = mbar_wait(p_full + t, j & 1, a.status, kSitePFull))) break;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || !uses(t, j)) continue;
+          if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull))) break;
           tc_fence_after_sync();
           const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             umma_ts(tmem + C::O_COL + D * t, tmem + 128 * t + kk * 8,
                     smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+                    (j > jb[t] || kk > 0) ? 1u : 0u);
           }
           umma_commit(pv_done + t);
         }
@@ -250,15 +286,20 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * t;
     const uint32_t tO = tmem + lane_off + C::O_COL + D * t;
-    const int nk = n_kv[t];
+    const int nk = t == 0 ? n_kv[0] : n_kv[1];   // selects, not a dynamic index (keeps them in registers)
+    const int jb_t = t == 0 ? jb[0] : jb[1];
     const float sl2 = a.scale_log2;
-    // key j is visible to this row iff j <= vis_last
-    const int vis_last = a.causal ? min(a.Nk - 1, row + a.causal_offset) : a.Nk - 1;
-    const int tile_first_vis = a.causal ? min(a.Nk - 1, q_base + 128 * t + a.causal_offset) : a.Nk - 1;
+    // keys this row sees: [vis_lo, vis_hi]; a key tile needs per-element masking
+    // when it crosses the left edge of the tile's last row or the right edge
+    // of its first row (the edges only move forward with the row)
+    int vis_lo, vis_hi, lo_last, hi_first, unused;
+    fwd_row_keys<WIN>(a, row, vis_lo, vis_hi);
+    fwd_row_keys<WIN>(a, min(q_base + 128 * t + 127, max(a.Nq - 1, 0)), lo_last, unused);
+    fwd_row_keys<WIN>(a, q_base + 128 * t, unused, hi_first);
     float m_used = -CUDART_INF_F;  // reference max, base-2 scaled units
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {
+    for (int j = 0; j < nk; ++j) {  // step j visits key tile jb[t] + j
       if (!(ok = mbar_wait(s_full + t, j & 1, a.status, kSiteSFull))) break;
       tc_fence_after_sync();
       float sv[128];
@@ -274,11 +315,12 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(sr[c][i]);
         }
       }
-      const int key0 = j * 128;
-      if (key0 + 127 > tile_first_vis) {  // tile-uniform: diagonal or ragged tail
-        const int rel = vis_last - key0;
+      const int key0 = (jb_t + j) * 128;
+      if (key0 + 127 > hi_first || (WIN && key0 < lo_last)) {  // tile-uniform: an edge crosses the tile
+        const int rel_lo = vis_lo - key0, rel_hi = vis_hi - key0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) sv[c] = (c > rel) ? -CUDART_INF_F : sv[c];
+        for (int c = 0; c < 128; ++c)
+          sv[c] = ((WIN && c < rel_lo) || c > rel_hi) ? -CUDART_INF_F : sv[c];
       }
       // Row max with three-input max (half the instructions of a pairwise
       // chain; four independent chains for latency).

@@ -84,6 +84,20 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      int Nq, int Nk, int d, float scale, int causal, void* stream);
 
 /*
+ * attn_fwd with a local (sliding) window ([AUT] §2, its Longformer
+ * comparison: local windows change which positions interact; [PW] §6.1:
+ * window attention costs O(n w)). Query i is aligned with key
+ * i + (Nk - Nq) and sees key j only if |j - (i + Nk - Nq)| < window; with
+ * causal = 1 also only j <= i + (Nk - Nq). window = 0 is no window (attn_fwd);
+ * window < 0 is ATTN_ERR_INVALID_ARG. Rows that see no key give o = 0,
+ * lse = -inf. Only the key tiles a query tile can see are read. Other
+ * arguments as attn_fwd.
+ */
+ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                     int Hkv, int Nq, int Nk, int d, float scale, int causal, int window,
+                                     void* stream);
+
+/*
  * Size in bytes of the device workspace attn_decode needs for these sizes
  * (split-KV partial results and one ticket per (sequence, KV head, query
  * group)). Returns 0 for arguments attn_decode would reject. The workspace

@@ -89,6 +89,12 @@ def test_fwd_argument_checks(lib, kw, code):
     assert _fwd(lib, **kw) == code
 
 
+def test_fwd_window_argument_checks(lib):
+    assert lib.attn_fwd_window(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 1, 16, 16, 64, 0.125, 1, -1, None) == \
+        binding.ERR_INVALID_ARG
+    assert lib.attn_fwd_window(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 1, 0, 16, 64, 0.125, 1, 8, None) == binding.OK
+
+
 def _dec(lib, q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Lmax=100, d=128,
          scale=0.1, ws=FAKE, wsb=1 << 30):
     return lib.attn_decode(q, kc, vc, sl, o, lse, B, Hq, Hkv, Lmax, d, scale, ws, wsb, None)

@@ -112,3 +112,43 @@ def test_full_size_sampled_rows(w):
                                                       vd[b:b + 1, hk:hk + 1], w.scale, w.causal, rows=rows)
             compare(o_cpu[b:b + 1, h:h + 1, rows], lse_cpu[b:b + 1, h:h + 1, rows], o_ref, lse_ref,
                     f"{w.name} b={b} h={h}")
+
+
+WINDOW_CASES = [
+    # (name, B, Hq, Hkv, Nq, Nk, d, causal, window)
+    ("win50_causal", 1, 4, 2, 700, 700, 128, True, 50),
+    ("win128_causal", 1, 4, 1, 600, 600, 128, True, 128),
+    ("win129_causal_d64", 2, 2, 2, 520, 520, 64, True, 129),
+    ("win1_causal", 1, 2, 2, 300, 300, 128, True, 1),
+    ("win300_noncausal", 1, 4, 2, 900, 900, 128, False, 300),
+    ("win64_noncausal_d64", 1, 4, 4, 333, 333, 64, False, 64),
+    ("win200_cross_nq300_nk1000", 1, 4, 2, 300, 1000, 128, True, 200),
+    ("win90_cross_nq500_nk200", 1, 2, 1, 500, 200, 64, True, 90),
+    ("win5000_wider_than_input", 1, 2, 2, 400, 400, 128, True, 5000),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=lambda c: c[0])
+def test_window_full_output(case):
+    name, B, Hq, Hkv, Nq, Nk, d, causal, window = case
+    w = Prefill(name, B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d, causal=causal, seed=60)
+    q, k, v = prefill_inputs(w)
+    o, lse = binding.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=w.scale, window=window)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention_forward(f64(q), f64(k), f64(v), w.scale, causal, window=window)
+    compare(o, lse, o_ref, lse_ref, name)
+    assert binding.device_status()[0] == binding.OK
+
+
+def test_window_full_size_sampled_rows():
+    """Causal GQA N=16384 with a 4096-key window, sampled rows across the sequence."""
+    w = CAUSAL_GQA_16384
+    q, k, v = prefill_inputs(w)
+    o, lse = binding.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=w.scale, window=4096)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 4095, 4096, 4097, 8191, 12345, 16383])
+    for h in (0, 7, 8, 63):
+        hk = h // (w.Hq // w.Hkv)
+        o_ref, lse_ref = oracle.attention_forward(f64(q[:, h:h + 1]), f64(k[:, hk:hk + 1]), f64(v[:, hk:hk + 1]),
+                                                  w.scale, True, rows=rows, window=4096)
+        compare(o[:, h:h + 1, rows], lse[:, h:h + 1, rows], o_ref, lse_ref, f"window4096 head {h}")
