@@ -6,8 +6,9 @@
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
 already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
 N=16384, d=128), a decode step (B=16, Hq=32, Hkv=8, d=128, cache lengths
-uniform on [1024, 8192]) and the same decode over a paged cache (64-token
-pages) with the new token appended. L2 is flushed (a 256 MiB write) before each
+uniform on [1024, 8192]), the same decode over a paged cache (64-token
+pages) with the new token appended, and the prefill again with a 4096-key
+causal sliding window. L2 is flushed (a 256 MiB write) before each
 of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
 read so the timed kernel does not pay for writing back the flush's dirty lines.
 Prints one JSON line.
@@ -44,6 +45,7 @@ from exact_scaled_dot_03_b300 import workloads as W  # noqa: E402
 METRIC = "attn fwd TFLOP/s (bf16, causal) and decode GB/s; % of B300 roofline"
 PREFILL = {w.name: w for w in W.PREFILL_WORKLOADS}
 L2_FLUSH_BYTES = 256 << 20
+WINDOW = 4096  # local-window width of the sliding-window prefill measured beside the full one
 
 
 # ---------------------------------------------------------------- helpers
@@ -248,6 +250,7 @@ def run_ours(args, w, wd):
     do_pre = args.only in (None, "prefill")
     do_dec = args.only in (None, "decode")
     do_pag = args.only in (None, "paged")
+    do_win = args.only in (None, "window")
 
     parts = []  # (name, launch function)
     if do_pre:
@@ -264,6 +267,15 @@ def run_ours(args, w, wd):
         ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
         parts.append(("decode", lambda: binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do,
                                                        lse=dlse)))
+    if do_win:
+        ww = W.CAUSAL_GQA_16384
+        if not do_pre:
+            q_h, k_h, v_h = W.prefill_inputs(ww)
+            q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+            o = torch.empty_like(q)
+            lse = torch.empty(ww.B, ww.Hq, ww.Nq, dtype=torch.float32, device=dev)
+        parts.append(("window", lambda: binding.fwd(q, k, v, causal=True, scale=ww.scale, out=o, lse=lse,
+                                                    window=WINDOW)))
     if do_pag:
         wp = W.DECODE_GQA_PAGED
         pq_h, pkn_h, pvn_h, pkp_h, pvp_h, pbt_h, psl_h = W.paged_decode_inputs(wp)
@@ -360,6 +372,22 @@ def run_ours(args, w, wd):
                      "ms": tot["decode"] / args.steps, "roofline": dec_roof}
         if not do_pre:   # decode alone: its numbers are the line's
             value, unit, roofline = dec_value, "GB/s", dec_roof
+    win_block = None
+    if do_win:
+        # FLOPs of the pairs that are actually visible: row i sees min(i+1, WINDOW) keys
+        pairs = sum(min(i + 1, WINDOW) for i in range(ww.Nq))
+        win_flops = 4.0 * ww.B * ww.Hq * ww.d * pairs
+        win_value = world * win_flops * args.steps / (tot["window"] / 1e3) / 1e12
+        win_achieved = win_flops / (statistics.mean(ms["window"]) / 1e3) / 1e12
+        win_roof = {"bound": "tensor", "achieved": win_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": win_achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                    "traffic": None, "algorithmic_flops_per_launch": win_flops,
+                    "kernel": "attn_fwd_kernel<128, window>"}
+        win_block = {"metric": "causal sliding-window prefill TFLOP/s (visible pairs only)",
+                     "workload": f"{ww.name}_window{WINDOW}", "value": win_value, "unit": "TFLOP/s",
+                     "ms": tot["window"] / args.steps, "roofline": win_roof}
+        if not (do_pre or do_dec or do_pag):
+            value, unit, roofline = win_value, "TFLOP/s", win_roof
     pag_block = None
     if do_pag:
         pag_bytes = ((int(psl_h.sum()) + wp.B) * wp.Hkv * wp.d * 2 * 2 + 2 * wp.B * wp.Hq * wp.d * 2
@@ -391,7 +419,8 @@ def run_ours(args, w, wd):
             "warmup": args.warmup, "ms_per_step": sum(tot.values()) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16)",
-            "config": {"workload": w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name,
+            "config": {"workload": (w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name if do_pag
+                                    else f"{W.CAUSAL_GQA_16384.name}_window{WINDOW}"),
                        "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         }
@@ -404,6 +433,8 @@ def run_ours(args, w, wd):
             line["decode"] = dec_block
         if pag_block is not None and (do_pre or do_dec):
             line["decode_paged"] = pag_block
+        if win_block is not None and (do_pre or do_dec or do_pag):
+            line["prefill_window"] = win_block
         line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
                      "clocks": clocks, "wall_s_timed_region": t_wall})
         print(json.dumps(line), flush=True)
@@ -456,7 +487,7 @@ def main():
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window"], default=None,
                     help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
