@@ -34,6 +34,9 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_decode,
     attention_decode_paged,
+    attention_forward_rope,
+    rope_rotate,
+    round_to_bf16,
     online_attention_rows,
     merge_two_blocks,
     score_bytes,

@@ -129,6 +129,50 @@ def attention_decode(q, k_cache, v_cache, seqlens, scale: float):
     return o, lse
 
 
+def rope_rotate(x, positions, base: float = 10000.0):
+    """Rotary position embedding of [..., n, d] vectors ([PW] §5.3).
+
+    The d components are split into pairs (2i, 2i+1); the pair of a vector at
+    position m is rotated by the angle m * base**(-2i/d):
+        x'_{2i}   = x_{2i} cos(theta) - x_{2i+1} sin(theta)
+        x'_{2i+1} = x_{2i} sin(theta) + x_{2i+1} cos(theta)
+    so that the score of a query at m and a key at n depends on m - n only.
+    positions: [n] integers. fp64 throughout.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    i = np.arange(d // 2)
+    theta = np.asarray(positions, dtype=np.float64)[:, None] * base ** (-2.0 * i / d)[None, :]
+    c, s = np.cos(theta), np.sin(theta)
+    out = np.empty_like(x)
+    out[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+    out[..., 1::2] = x[..., 0::2] * s + x[..., 1::2] * c
+    return out
+
+
+def round_to_bf16(x):
+    """fp64 -> nearest bf16 value (ties to even), returned as fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
+    out = rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+    return np.where(np.isfinite(f), out, f.astype(np.float64))
+
+
+def attention_forward_rope(q, k, v, scale: float, causal: bool, base: float = 10000.0, window: int = 0):
+    """Prefill with RoPE applied to Q and K first ([PW] §5.3: it acts on Q
+    and K, not on the input). Key j sits at position j and query i at
+    position i + (Nk - Nq), the same alignment as the causal rule. The
+    rotated Q and K are rounded to bf16 (the inputs' type) before the scores,
+    then the plain definition (attention_forward) is applied."""
+    Nq, Nk = q.shape[-2], k.shape[-2]
+    qr = round_to_bf16(rope_rotate(q, np.arange(Nq) + (Nk - Nq), base))
+    kr = round_to_bf16(rope_rotate(k, np.arange(Nk), base))
+    return attention_forward(qr, kr, v, scale, causal, window=window)
+
+
 def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale: float, k_new=None, v_new=None):
     """Decode step over a paged KV cache, with the new token's K/V appended first.
 

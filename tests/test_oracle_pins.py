@@ -15,6 +15,9 @@ import pytest
 import torch
 
 from oracle import (
+    attention_forward_rope,
+    rope_rotate,
+    round_to_bf16,
     attention_decode_paged,
     attention_decode,
     attention_forward,
@@ -484,3 +487,53 @@ def test_window_of_one_sees_only_the_aligned_key():
     o, lse = attention_forward(q, k, v, 1.0, True, window=1)
     np.testing.assert_allclose(o[0], v[0], atol=1e-15)
     np.testing.assert_allclose(lse[0], np.einsum("hid,hid->hi", q[0], k[0]), atol=1e-12)
+
+
+# --- rotary position embedding -----------------------------------------------------------------
+
+def test_rope_scores_depend_only_on_relative_position():
+    """[PW] §5.3: with RoPE the score of a query at m and a key at n depends
+    only on m - n. Shift both positions by the same amount: same scores."""
+    rng = np.random.default_rng(70)
+    d = 16
+    q, k = _rand(rng, 1, d), _rand(rng, 1, d)
+    for m, n in [(5, 2), (100, 40), (7, 7)]:
+        s0 = rope_rotate(q, [m]) @ rope_rotate(k, [n]).T
+        for shift in (1, 37, 1000):
+            s1 = rope_rotate(q, [m + shift]) @ rope_rotate(k, [n + shift]).T
+            np.testing.assert_allclose(s1, s0, atol=1e-10)
+
+
+def test_rope_is_a_pairwise_rotation():
+    """Position 0 is the identity; each pair keeps its norm; pair 0 at position 1
+    turns by exactly one radian (omega_0 = 1); a quarter turn maps (x, y) to (-y, x)."""
+    rng = np.random.default_rng(71)
+    x = _rand(rng, 3, 8)
+    np.testing.assert_array_equal(rope_rotate(x, [0, 0, 0]), x)
+    r = rope_rotate(x, [3, 9, 250])
+    np.testing.assert_allclose(np.hypot(r[:, 0::2], r[:, 1::2]), np.hypot(x[:, 0::2], x[:, 1::2]), atol=1e-12)
+    e = np.zeros((1, 8)); e[0, 0] = 1.0
+    np.testing.assert_allclose(rope_rotate(e, [1])[0, :2], [math.cos(1.0), math.sin(1.0)], atol=1e-15)
+    # base chosen so that pair 1 of d=4 turns by pi/2 at position 1: base^(-2/4) = pi/2
+    b = (math.pi / 2) ** -2
+    v = np.array([[0.0, 0.0, 3.0, 5.0]])
+    np.testing.assert_allclose(rope_rotate(v, [1], base=b)[0, 2:], [-5.0, 3.0], atol=1e-12)
+
+
+def test_rope_attention_matches_rotating_by_hand_and_rounding():
+    rng = np.random.default_rng(72)
+    B, Hq, Hkv, Nq, Nk, d = 1, 4, 2, 9, 13, 8
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    o, lse = attention_forward_rope(q, k, v, 0.3, True)
+    theta_q = (np.arange(Nq) + Nk - Nq)[:, None] * 10000.0 ** (-np.arange(0, d, 2) / d)[None, :]
+    qr = q.copy()
+    qr[..., 0::2] = q[..., 0::2] * np.cos(theta_q) - q[..., 1::2] * np.sin(theta_q)
+    qr[..., 1::2] = q[..., 0::2] * np.sin(theta_q) + q[..., 1::2] * np.cos(theta_q)
+    qr = torch.from_numpy(qr).to(torch.bfloat16).double().numpy()  # RNE to bf16 by torch
+    kr = torch.from_numpy(rope_rotate(k, np.arange(Nk))).to(torch.bfloat16).double().numpy()
+    o2, lse2 = attention_forward(qr, kr, v, 0.3, True)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    # the rounding helper agrees with torch's bf16 conversion bit for bit
+    x = rng.standard_normal(10000) * 10 ** rng.uniform(-3, 3, 10000)
+    np.testing.assert_array_equal(round_to_bf16(x), torch.from_numpy(x).float().to(torch.bfloat16).double().numpy())
