@@ -24,6 +24,8 @@ _vp, _i, _f, _sz, _i64, _u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, c
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "attn_fwd_rope_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "attn_fwd_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _vp, _sz, _vp]),
     "attn_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
@@ -116,6 +118,31 @@ def fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, w
                                  lse.data_ptr() if lse is not None else None,
                                  B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)), int(window), _stream_handle(stream))
     _check(code, "attn_fwd_window")
+    return o, lse
+
+
+def fwd_rope(q, k, v, causal: bool, scale: float | None = None, window: int = 0, base: float = 10000.0,
+             workspace=None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Prefill with RoPE on Q and K: returns (o, lse); see ``attn_fwd_rope`` in include/attn.h."""
+    _need(q, "q", dims=4)
+    _need(k, "k", dims=4)
+    _need(v, "v", dims=4)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if workspace is None:
+        n = int(lib().attn_fwd_rope_workspace_size(B, Hkv, Nq, Nk, d))
+        if n == 0:
+            raise AttnError(ERR_UNSUPPORTED, "attn_fwd_rope_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    s = default_scale(d) if scale is None else float(scale)
+    code = lib().attn_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Nq, Nk, d, s,
+                               int(bool(causal)), int(window), float(base), workspace.data_ptr(), workspace.numel(),
+                               _stream_handle(stream))
+    _check(code, "attn_fwd_rope")
     return o, lse
 
 

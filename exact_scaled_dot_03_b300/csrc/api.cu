@@ -14,6 +14,7 @@
 #include "attn.h"
 #include "decode_kernel.cuh"
 #include "fwd_kernel.cuh"
+#include "rope_kernel.cuh"
 
 namespace {
 
@@ -92,7 +93,8 @@ __global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, size_t rows, int
 
 template <int D>
 attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream, int dev) {
+                       int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream, int dev,
+                       const float2* rope_cs = nullptr, int rope_pmin = 0, int rope_T = 0) {
   static bool smem_set[kMaxDevices] = {};
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -116,6 +118,9 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.causal = causal;
   a.causal_offset = Nk - Nq;
   a.window = window;
+  a.rope_cs = rope_cs;
+  a.rope_pmin = rope_pmin;
+  a.rope_T = rope_T;
   a.num_pairs = (Nq + 255) / 256;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = status_ptr(dev);
@@ -277,6 +282,77 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
   }
   if (d == 64) return launch_fwd<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev);
   return launch_fwd<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev);
+}
+
+namespace {
+// RoPE workspace: the rotated K ([B, Hkv, Nk, d] bf16), then the (cos, sin)
+// table of positions min(0, Nk - Nq) .. Nk - 1, position-major and pair-major.
+struct RopePlan {
+  size_t k_bytes, cs_off, cst_off, total;
+  int T, pmin;
+};
+bool plan_rope(int B, int Hkv, int Nq, int Nk, int d, RopePlan* p) {
+  if (B < 1 || Hkv < 1 || Nq < 0 || Nk < 1 || (d != 64 && d != 128)) return false;
+  p->pmin = Nk - Nq < 0 ? Nk - Nq : 0;
+  p->T = Nk - p->pmin;
+  p->k_bytes = static_cast<size_t>(B) * Hkv * Nk * d * 2;
+  p->cs_off = (p->k_bytes + 255) & ~size_t(255);
+  const size_t cs_bytes = static_cast<size_t>(p->T) * (d / 2) * sizeof(float2);
+  p->cst_off = (p->cs_off + cs_bytes + 255) & ~size_t(255);
+  p->total = p->cst_off + cs_bytes;
+  return true;
+}
+}  // namespace
+
+size_t attn_fwd_rope_workspace_size(int B, int Hkv, int Nq, int Nk, int d) {
+  RopePlan p;
+  return plan_rope(B, Hkv, Nq, Nk, d, &p) ? p.total : 0;
+}
+
+attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, float scale, int causal, int window, float rope_base,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (!std::isfinite(rope_base) || !(rope_base > 1.f) || workspace == nullptr || !aligned(workspace, 256))
+    return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || k == nullptr || v == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 1 || Hq % Hkv != 0 || window < 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || (Nq + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  RopePlan rp;
+  if (!plan_rope(B, Hkv, Nq, Nk, d, &rp)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < rp.total) return ATTN_ERR_INVALID_ARG;
+  if (Nq == 0) return ATTN_OK;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* k_rot = reinterpret_cast<__nv_bfloat16*>(ws);
+  float2* cs = reinterpret_cast<float2*>(ws + rp.cs_off);
+  float2* cs_t = reinterpret_cast<float2*>(ws + rp.cst_off);
+  RopeArgs ra;
+  ra.cs = cs;
+  ra.cs_t = cs_t;
+  ra.T = rp.T;
+  ra.pmin = rp.pmin;
+  for (int i = 0; i < d / 2; ++i) ra.w[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / d);
+  const int sms = sm_count(dev);
+  if (sms == 0) return ATTN_ERR_CUDA;
+  const long long rows = static_cast<long long>(B) * Hkv * Nk;
+  if (d == 64) {
+    rope_table_kernel<64><<<sms * 4, 256, 0, s>>>(ra);
+    rope_k_kernel<64><<<sms * 8, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k), k_rot, cs, rows, Nk, rp.pmin);
+  } else {
+    rope_table_kernel<128><<<sms * 4, 256, 0, s>>>(ra);
+    rope_k_kernel<128><<<sms * 8, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k), k_rot, cs, rows, Nk, rp.pmin);
+  }
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (d == 64) return launch_fwd<64>(q, k_rot, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev, cs_t, rp.pmin, rp.T);
+  return launch_fwd<128>(q, k_rot, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev, cs_t, rp.pmin, rp.T);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d) {

@@ -44,6 +44,12 @@ struct FwdArgs {
   int num_pairs;      // ceil(Nq / 256)
   float scale_log2;   // scale * log2(e)
   unsigned* status;   // library status word (see kStatus*)
+  // RoPE ([PW] §5.3): when rope_cs is set, K has already been rotated and the
+  // Q tiles are rotated in shared memory right after they land; rope_cs holds
+  // (cos, sin) as [D/2 pairs][rope_T positions from rope_pmin]. Query i sits
+  // at position i + causal_offset.
+  const float2* rope_cs;
+  int rope_pmin, rope_T;
 };
 
 template <int D>
@@ -60,7 +66,7 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain
-  static constexpr int NUM_BARS = 1 + 4 * STAGES + 7;
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 8;  // + q_ready
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + tmem base/abort words + alignment slack
   static constexpr int THREADS = 320;
@@ -127,6 +133,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_full + 2;           // [2]
   uint64_t* pv_done = p_full + 2;          // [2]
   uint64_t* drain = pv_done + 2;
+  uint64_t* q_ready = drain + 1;  // RoPE only: both Q tiles rotated in shared memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -163,6 +170,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(pv_done + t, 1);
     }
     mbar_init(drain, 1);
+    mbar_init(q_ready, 256);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && n_kv_max > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      bool ok = mbar_wait(q_full, 0, a.status, kSiteQFull);
+      bool ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull);
       for (int js = 0; ok && js < n_kv_max; ++js) {
         const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
         const int s = js % C::STAGES;
@@ -299,7 +307,38 @@ __global__ void __launch_bounds__(320, 1)
     float m_used = -CUDART_INF_F;  // reference max, base-2 scaled units
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {  // step j visits key tile jb[t] + j
+    if (a.rope_cs != nullptr) {
+      // RoPE on this thread's Q row, in place in the swizzled tile: pair p of
+      // chunk c (8 components) is the 32-bit word p of the chunk.
+      if (nk > 0 && row < a.Nq) {
+        // The row's (cos, sin) pairs are fetched before Q lands, so the loads
+        // overlap the Q copy instead of following it; the table is pair-major,
+        // so the warp's 32 consecutive rows read 256 contiguous bytes per pair.
+        const float2* tab = a.rope_cs + (row + a.causal_offset - a.rope_pmin);
+        float2 cs[D / 2];
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) cs[i] = __ldg(tab + (size_t)i * a.rope_T);
+        if (!(ok = mbar_wait(q_full, 0, a.status, kSiteQFull))) *abort_flag = 1;
+        const int rloc = wq * 32 + lane;
+        uint8_t* qrow = sQ + t * C::TILE_BYTES + rloc * 128;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4* p = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::BLOCK_BYTES + (((c & 7) ^ (rloc & 7)) << 4));
+          const uint4 w = *p;
+          uint32_t in[4] = {w.x, w.y, w.z, w.w}, out[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const float x = __uint_as_float(in[k2] << 16), y = __uint_as_float(in[k2] & 0xffff0000u);
+            const float2 t2 = cs[4 * c + k2];
+            out[k2] = pack_bf16x2(x * t2.x - y * t2.y, x * t2.y + y * t2.x);
+          }
+          if (ok) *p = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        fence_proxy_async_smem();  // the MMA reads Q through the async proxy
+      }
+      mbar_arrive(q_ready);
+    }
+    for (int j = 0; ok && j < nk; ++j) {  // step j visits key tile jb[t] + j
       if (!(ok = mbar_wait(s_full + t, j & 1, a.status, kSiteSFull))) break;
       tc_fence_after_sync();
       float sv[128];

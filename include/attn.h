@@ -98,6 +98,32 @@ ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v
                                      void* stream);
 
 /*
+ * Workspace bytes attn_fwd_rope needs: the rotated K ([B, Hkv, Nk, d] bf16)
+ * and a (cos, sin) table of max(Nk, Nq) positions x d/2 pairs (fp32).
+ * 0 for arguments attn_fwd_rope would reject.
+ */
+ATTN_API size_t attn_fwd_rope_workspace_size(int B, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * attn_fwd_window with rotary position embedding applied to Q and K first
+ * ([PW] §5.3): the components of each vector are split into pairs (2i, 2i+1)
+ * and the pair of a vector at position m is rotated by m * base^(-2i/d), so
+ * that scores depend only on relative position. Key j sits at position j and
+ * query i at position i + (Nk - Nq). The rotated Q and K are rounded to bf16.
+ * K is rotated once into the workspace (two small kernels: the (cos, sin)
+ * table, then K); each Q tile is rotated inside the prefill kernel right
+ * after it is loaded. q and k are not modified.
+ *
+ *   rope_base  > 1 and finite (10000 in the pages).
+ *   workspace  >= attn_fwd_rope_workspace_size(B, Hkv, Nq, Nk, d) bytes,
+ *              256-byte aligned, contents irrelevant (overwritten).
+ * Other arguments as attn_fwd_window (Nk must be >= 1).
+ */
+ATTN_API attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                   int Hkv, int Nq, int Nk, int d, float scale, int causal, int window,
+                                   float rope_base, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Size in bytes of the device workspace attn_decode needs for these sizes
  * (split-KV partial results and one ticket per (sequence, KV head, query
  * group)). Returns 0 for arguments attn_decode would reject. The workspace

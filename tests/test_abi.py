@@ -141,6 +141,26 @@ def test_paged_decode_argument_checks(lib, kw, code):
     assert _paged(lib, **kw) == code
 
 
+def test_fwd_rope_argument_checks(lib):
+    f = lambda **kw: lib.attn_fwd_rope(*[kw.get(n, dflt) for n, dflt in [
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("o", FAKE), ("lse", None), ("B", 1), ("Hq", 2), ("Hkv", 1),
+        ("Nq", 16), ("Nk", 16), ("d", 64), ("scale", 0.125), ("causal", 1), ("window", 0), ("base", 10000.0),
+        ("ws", 0x100000), ("wsb", 1 << 30), ("stream", None)]])
+    assert f(base=1.0) == binding.ERR_INVALID_ARG
+    assert f(base=float("nan")) == binding.ERR_INVALID_ARG
+    assert f(ws=None) == binding.ERR_INVALID_ARG
+    assert f(ws=0x100010) == binding.ERR_INVALID_ARG          # not 256-byte aligned
+    assert f(wsb=64) == binding.ERR_INVALID_ARG
+    assert f(Nk=0) == binding.ERR_INVALID_ARG
+    assert f(window=-2) == binding.ERR_INVALID_ARG
+    assert f(d=96) == binding.ERR_UNSUPPORTED
+    assert f(Nq=0) == binding.OK
+    # rotated K (1 x 1 x 16 x 64 bf16 = 2 KiB), then the 16 positions x 32 pairs
+    # x 8-byte (cos, sin) table twice: position-major and pair-major
+    assert lib.attn_fwd_rope_workspace_size(1, 1, 16, 16, 64) == 2048 + 2 * 16 * 32 * 8
+    assert lib.attn_fwd_rope_workspace_size(1, 1, 20, 16, 64) == 2048 + 2 * 20 * 32 * 8  # queries before key 0
+
+
 def test_paged_workspace_size(lib):
     # same plan as the contiguous decode with Lmax = pages * page_size
     assert binding.lib().attn_decode_paged_workspace_size(16, 32, 8, 128, 64, 128) == \

@@ -152,3 +152,45 @@ def test_window_full_size_sampled_rows():
         o_ref, lse_ref = oracle.attention_forward(f64(q[:, h:h + 1]), f64(k[:, hk:hk + 1]), f64(v[:, hk:hk + 1]),
                                                   w.scale, True, rows=rows, window=4096)
         compare(o[:, h:h + 1, rows], lse[:, h:h + 1, rows], o_ref, lse_ref, f"window4096 head {h}")
+
+
+ROPE_CASES = [
+    # (name, B, Hq, Hkv, Nq, Nk, d, causal, window)
+    ("rope_causal_gqa_n333", 1, 8, 2, 333, 333, 128, True, 0),
+    ("rope_noncausal_d64_n384", 2, 4, 4, 384, 384, 64, False, 0),
+    ("rope_cross_nq200_nk520", 1, 4, 2, 200, 520, 128, True, 0),
+    ("rope_cross_nq300_nk130_d64", 1, 2, 2, 300, 130, 64, True, 0),
+    ("rope_window100", 1, 4, 1, 700, 700, 128, True, 100),
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=lambda c: c[0])
+def test_rope_full_output(case):
+    name, B, Hq, Hkv, Nq, Nk, d, causal, window = case
+    w = Prefill(name, B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d, causal=causal, seed=61)
+    q, k, v = prefill_inputs(w)
+    qd, kd = q.to(DEV), k.to(DEV)
+    o, lse = binding.fwd_rope(qd, kd, v.to(DEV), causal=causal, scale=w.scale, window=window)
+    torch.cuda.synchronize()
+    assert torch.equal(qd.cpu(), q) and torch.equal(kd.cpu(), k)  # inputs untouched
+    o_ref, lse_ref = oracle.attention_forward_rope(f64(q), f64(k), f64(v), w.scale, causal, window=window)
+    compare(o, lse, o_ref, lse_ref, name)
+    assert binding.device_status()[0] == binding.OK
+
+
+def test_rope_full_size_sampled_rows():
+    """Causal GQA N=16384 with RoPE: positions up to 16383 (angles ~1.6e4 rad)."""
+    w = CAUSAL_GQA_16384
+    q, k, v = prefill_inputs(w)
+    o, lse = binding.fwd_rope(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 5000, 8191, 12345, 16383])
+    for h in (0, 9, 63):
+        hk = h // (w.Hq // w.Hkv)
+        # RoPE of the whole K head (all positions) and of the sampled query rows
+        kr = oracle.round_to_bf16(oracle.rope_rotate(f64(k[:, hk:hk + 1]), np.arange(w.Nk)))
+        qr = oracle.round_to_bf16(oracle.rope_rotate(f64(q[:, h:h + 1, rows]), rows))
+        qfull = np.zeros((1, 1, w.Nq, w.d))
+        qfull[:, :, rows] = qr
+        o_ref, lse_ref = oracle.attention_forward(qfull, kr, f64(v[:, hk:hk + 1]), w.scale, True, rows=rows)
+        compare(o[:, h:h + 1, rows], lse[:, h:h + 1, rows], o_ref, lse_ref, f"rope head {h}")
