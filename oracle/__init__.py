@@ -23,7 +23,7 @@ and section:
          prefill/decode section (decode reads cached K/V).
   [PW]   pwwt.cn news 6124947 (Transformer algorithm-evolution article) --
          §2.1 S = QK^T/sqrt(d_k), §2.3 MQA/GQA, §3.1-3.2 KV cache and its
-         size, §4.2 online softmax is exact.
+         size, §4.2 online softmax is exact, §5.3 RoPE, §6.1 sliding window.
 
 Parity status: every public function here is pinned by ``tests/test_oracle_pins.py``
 against facts other than itself (closed forms, invariants, the pages' worked
@@ -33,6 +33,7 @@ from .attention import (  # noqa: F401
     bf16_bits_to_f64,
     attention_forward,
     attention_decode,
+    attention_backward,
     attention_decode_paged,
     attention_forward_rope,
     rope_rotate,

@@ -102,6 +102,73 @@ def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block:
     return o, lse
 
 
+def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_rows=None, row_block: int = 1024):
+    """Gradients of O = softmax(scale * Q K^T + mask) V with respect to Q, K, V.
+
+    Given dO = dL/dO for some loss L, returns (dq, dk, dv) = dL/dQ, dL/dK,
+    dL/dV. The pages name the backward pass as the reason the score matrix is
+    stored in standard attention ([MG-A] §3.3) and say the tiled method
+    instead recomputes it from Q and K ([MG-B] §3.2, engineering results);
+    the exact tiled method is to be checked on its gradients as well as its
+    outputs ([AUT] method table, exact tiled attention row; verification
+    protocol, second step). They give no formulas, so this is the chain rule
+    through the forward definition, written out:
+
+      S = scale * Q K^T (masked entries -inf), P = row softmax(S), O = P V
+      dV = P^T dO                      (O is linear in V)
+      dP = dO V^T
+      dS_ij = P_ij * (dP_ij - sum_k P_ik dP_ik)   (Jacobian of a row softmax)
+      dQ = scale * dS K,  dK = scale * dS^T Q
+
+    With GQA the query heads of a group share one K/V head, so their dK and
+    dV contributions add. Masked entries have P = 0, hence dS = 0; a row with
+    no visible key contributes nothing and gets dq = 0.
+
+    q, do: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (float64). q_rows / k_rows
+    select which query rows of dq and which key rows of dk, dv are returned
+    (all by default); every query row's full score vector is still
+    materialised, in blocks of ``row_block`` rows, before its softmax.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, dv_ = v.shape
+    assert k.shape == (B, Hkv, Nk, d) and do.shape == (B, Hq, Nq, dv_) and Hq % Hkv == 0
+    q_rows = np.arange(Nq) if q_rows is None else np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.arange(Nk) if k_rows is None else np.asarray(k_rows, dtype=np.int64)
+    dq = np.zeros((B, Hq, q_rows.size, d))
+    dk = np.zeros((B, Hkv, k_rows.size, d))
+    dv = np.zeros((B, Hkv, k_rows.size, dv_))
+    keys = np.arange(Nk)
+    want_q = np.zeros(Nq, dtype=bool)
+    want_q[q_rows] = True
+    q_pos = np.full(Nq, -1)
+    q_pos[q_rows] = np.arange(q_rows.size)
+    for b in range(B):
+        for h in range(Hq):
+            g = _kv_head(h, Hq, Hkv)
+            kh, vh = k[b, g], v[b, g]
+            for r0 in range(0, Nq, row_block):
+                ri = np.arange(r0, min(Nq, r0 + row_block))
+                if k_rows.size == 0 and not want_q[ri].any():
+                    continue
+                S = scale * (q[b, h, ri] @ kh.T)
+                if causal:
+                    S = np.where(keys[None, :] > ri[:, None] + (Nk - Nq), -np.inf, S)
+                P, _ = _two_pass_softmax(S)
+                dP = do[b, h, ri] @ vh.T
+                dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                sel = want_q[ri]
+                if sel.any():
+                    dq[b, h, q_pos[ri[sel]]] = scale * (dS[sel] @ kh)
+                if k_rows.size:
+                    dv[b, g] += P[:, k_rows].T @ do[b, h, ri]
+                    dk[b, g] += scale * (dS[:, k_rows].T @ q[b, h, ri])
+    return dq, dk, dv
+
+
 def attention_decode(q, k_cache, v_cache, seqlens, scale: float):
     """One decode step: each sequence's new query attends to its cached keys.
 

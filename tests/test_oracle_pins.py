@@ -20,6 +20,7 @@ from oracle import (
     round_to_bf16,
     attention_decode_paged,
     attention_decode,
+    attention_backward,
     attention_forward,
     bf16_bits_to_f64,
     kv_cache_bytes,
@@ -537,3 +538,116 @@ def test_rope_attention_matches_rotating_by_hand_and_rounding():
     # the rounding helper agrees with torch's bf16 conversion bit for bit
     x = rng.standard_normal(10000) * 10 ** rng.uniform(-3, 3, 10000)
     np.testing.assert_array_equal(round_to_bf16(x), torch.from_numpy(x).float().to(torch.bfloat16).double().numpy())
+
+
+# ---------------------------------------------------------------- backward pass
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 2, 2, 9, 9, 4, False),
+    (2, 4, 2, 13, 13, 8, True),      # GQA: the group's dK, dV contributions add
+    (1, 3, 1, 6, 11, 5, True),       # MQA, bottom-right causal with Nq < Nk
+    (1, 2, 1, 12, 7, 8, False),      # cross-attention, Nq > Nk
+])
+def test_backward_matches_torch_autograd_fp64(B, Hq, Hkv, Nq, Nk, d, causal):
+    """torch autograd through its own matmul / masked softmax (fp64) is an
+    independent derivation of the same gradients."""
+    rng = np.random.default_rng(40 + Nq)
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    do = _rand(rng, B, Hq, Nq, d)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = attention_backward(q, k, v, do, scale, causal)
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (q, k, v))
+    g = Hq // Hkv
+    s = torch.einsum("bhid,bhjd->bhij", tq, tk.repeat_interleave(g, dim=1)) * scale
+    if causal:
+        keep = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+        s = s.masked_fill(~keep, -math.inf)
+    o = torch.softmax(s, dim=-1) @ tv.repeat_interleave(g, dim=1)
+    o.backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+def test_backward_equals_central_finite_differences():
+    """Brute force: perturb every input entry of L = sum(dO * O) and difference
+    the forward definition."""
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 1, 3, 4, 3
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    do = _rand(rng, B, Hq, Nq, d)
+    scale = 0.7
+    dq, dk, dv = attention_backward(q, k, v, do, scale, True)
+
+    def loss(qq, kk, vv):
+        return float((attention_forward(qq, kk, vv, scale, True)[0] * do).sum())
+
+    eps = 1e-6
+    for x, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(grad, num, atol=1e-8)
+
+
+def test_backward_shift_and_sum_invariants():
+    """Adding one vector to every key leaves each softmax row unchanged, so
+    sum_j dK_j = 0; each row of P sums to 1, so sum_j dV_j = sum_i dO_i over
+    rows that see a key; identical keys make every row uniform, so dQ = 0."""
+    rng = np.random.default_rng(42)
+    B, Hq, Hkv, Nq, Nk, d = 2, 4, 2, 17, 23, 8
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    do = _rand(rng, B, Hq, Nq, d)
+    for causal in (False, True):
+        dq, dk, dv = attention_backward(q, k, v, do, 0.4, causal)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+        do_sum = do.reshape(B, Hkv, Hq // Hkv, Nq, d).sum(axis=(2, 3))
+        np.testing.assert_allclose(dv.sum(axis=2), do_sum, atol=1e-12)
+    k_same = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    dq, _, _ = attention_backward(q, k_same, v, do, 0.4, False)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+
+
+def test_backward_empty_rows_and_linearity_in_do():
+    rng = np.random.default_rng(43)
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 1, 9, 5, 4   # causal, Nq > Nk: rows 0..3 see no key
+    q, k, v = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    do1, do2 = _rand(rng, B, Hq, Nq, d), _rand(rng, B, Hq, Nq, d)
+    g1 = attention_backward(q, k, v, do1, 0.5, True)
+    np.testing.assert_array_equal(g1[0][:, :, :Nq - Nk], 0.0)
+    g2 = attention_backward(q, k, v, do2, 0.5, True)
+    g12 = attention_backward(q, k, v, 2.0 * do1 - 3.0 * do2, 0.5, True)
+    for a, b_, c in zip(g1, g2, g12):
+        np.testing.assert_allclose(c, 2.0 * a - 3.0 * b_, atol=1e-12)
+
+
+def test_backward_row_subsets_are_exact():
+    rng = np.random.default_rng(44)
+    q, k, v = _rand(rng, 1, 4, 40, 8), _rand(rng, 1, 2, 40, 8), _rand(rng, 1, 2, 40, 8)
+    do = _rand(rng, 1, 4, 40, 8)
+    full = attention_backward(q, k, v, do, 0.35, True, row_block=9)
+    qr, kr = np.array([0, 5, 39]), np.array([1, 20, 38, 39])
+    dq, dk, dv = attention_backward(q, k, v, do, 0.35, True, q_rows=qr, k_rows=kr, row_block=16)
+    np.testing.assert_allclose(dq, full[0][:, :, qr], atol=1e-13)
+    np.testing.assert_allclose(dk, full[1][:, :, kr], atol=1e-13)
+    np.testing.assert_allclose(dv, full[2][:, :, kr], atol=1e-13)
+
+
+def test_sum_invariant_catches_a_dropped_softmax_correction():
+    """The invariants above are sensitive: leaving out the row term of the
+    softmax Jacobian (dS = P * dP) breaks sum_j dK_j = 0."""
+    rng = np.random.default_rng(45)
+    q, k, v = _rand(rng, 1, 1, 6, 4), _rand(rng, 1, 1, 6, 4), _rand(rng, 1, 1, 6, 4)
+    do = _rand(rng, 1, 1, 6, 4)
+    S = 0.5 * q[0, 0] @ k[0, 0].T
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    wrong_dk = 0.5 * (P * (do[0, 0] @ v[0, 0].T)).T @ q[0, 0]
+    assert np.abs(wrong_dk.sum(axis=0)).max() > 1e-3
+    _, dk, _ = attention_backward(q, k, v, do, 0.5, False)
+    assert np.abs(dk[0, 0].sum(axis=0)).max() < 1e-12
