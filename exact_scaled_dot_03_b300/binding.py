@@ -26,6 +26,8 @@ SIGNATURES = {
     "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "attn_fwd_rope_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_fwd_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _vp, _sz, _vp]),
+    "attn_bwd_workspace_size": (_sz, [_i, _i, _i]),
+    "attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "attn_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
@@ -144,6 +146,28 @@ def fwd_rope(q, k, v, causal: bool, scale: float | None = None, window: int = 0,
                                _stream_handle(stream))
     _check(code, "attn_fwd_rope")
     return o, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, workspace=None, dq=None, dk=None, dv=None,
+        stream=None):
+    """Backward of ``fwd``: returns (dq, dk, dv); see ``attn_bwd`` in include/attn.h."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, name, dims=4)
+    _need(lse, "lse", dtype=torch.float32, dims=3)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if workspace is None:
+        n = int(lib().attn_bwd_workspace_size(B, Hq, Nq))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    s = default_scale(d) if scale is None else float(scale)
+    code = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)),
+                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(code, "attn_bwd")
+    return dq, dk, dv
 
 
 def decode_workspace_size(B: int, Hq: int, Hkv: int, Lmax: int, d: int) -> int:

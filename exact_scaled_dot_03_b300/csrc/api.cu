@@ -15,6 +15,7 @@
 #include "decode_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "rope_kernel.cuh"
+#include "bwd_kernel.cuh"
 
 namespace {
 
@@ -250,6 +251,60 @@ attn_status dispatch_decode_gc(const void* q, const void* kc, const void* vc, co
 
 }  // namespace
 
+namespace {
+// Backward workspace: (lse2, Dl) per query row, each head padded to 128 rows.
+bool plan_bwd(int B, int Hq, int Nq, int* Nq_pad, size_t* bytes) {
+  if (B < 1 || Hq < 1 || Nq < 0) return false;
+  *Nq_pad = (Nq + 127) / 128 * 128;
+  *bytes = static_cast<size_t>(B) * Hq * static_cast<size_t>(*Nq_pad) * sizeof(float2);
+  return true;
+}
+
+template <int D>
+attn_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                       void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
+                       float2* ld, int Nq_pad, cudaStream_t s, int dev) {
+  using C = BwdCfg<D>;
+  static bool smem_kv[kMaxDevices] = {}, smem_q[kMaxDevices] = {};
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, 128) ||
+      !make_map(&tdo, dout, D, Nq, static_cast<long long>(B) * Hq, 128) ||
+      !make_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, 128) ||
+      !make_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, 128))
+    return ATTN_ERR_CUDA;
+  if (!ensure_smem(attn_bwd_dkdv_kernel<D>, C::KV_SMEM_BYTES, dev, smem_kv) ||
+      !ensure_smem(attn_bwd_dq_kernel<D>, C::Q_SMEM_BYTES, dev, smem_q))
+    return ATTN_ERR_CUDA;
+  BwdArgs a;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.ld = ld;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.Nq_pad = Nq_pad;
+  a.group = Hq / Hkv;
+  a.causal = causal;
+  a.causal_offset = Nk - Nq;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.status = status_ptr(dev);
+  const int sms = sm_count(dev);
+  if (a.status == nullptr || sms == 0) return ATTN_ERR_CUDA;
+  const long long heads = static_cast<long long>(B) * Hq;
+  const long long threads = heads * Nq_pad * (D / 8);
+  const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
+  bwd_prep_kernel<D><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                            static_cast<const __nv_bfloat16*>(dout), lse, ld, heads, Nq, Nq_pad);
+  attn_bwd_dkdv_kernel<D><<<dim3(Hkv, (Nk + 127) / 128, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -353,6 +408,53 @@ attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, 
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   if (d == 64) return launch_fwd<64>(q, k_rot, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev, cs_t, rp.pmin, rp.T);
   return launch_fwd<128>(q, k_rot, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, s, dev, cs_t, rp.pmin, rp.T);
+}
+
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq) {
+  int pad;
+  size_t bytes;
+  return plan_bwd(B, Hq, Nq, &pad, &bytes) ? bytes : 0;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                     int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  // Tensors with no rows may be NULL (an empty tensor has no storage).
+  if (Nq > 0 && (q == nullptr || o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (Nk > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || (Nq + 127) / 128 > 65535 || (Nk + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
+  int Nq_pad;
+  size_t need;
+  if (!plan_bwd(B, Hq, Nq, &Nq_pad, &need)) return ATTN_ERR_INVALID_ARG;
+  if (Nq > 0 && Nk > 0 && (workspace == nullptr || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Nq == 0 || Nk == 0) {
+    // No query or no key: every gradient that exists is zero.
+    const size_t qrows = static_cast<size_t>(B) * Hq * Nq, krows = static_cast<size_t>(B) * Hkv * Nk;
+    const int qb = static_cast<int>(std::min<size_t>((qrows * d + 255) / 256, 148 * 16));
+    const int kb = static_cast<int>(std::min<size_t>((krows * d + 255) / 256, 148 * 16));
+    if (qrows > 0) fill_empty_kernel<<<qb, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), nullptr, qrows, d);
+    if (krows > 0) {
+      fill_empty_kernel<<<kb, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dk), nullptr, krows, d);
+      fill_empty_kernel<<<kb, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dv), nullptr, krows, d);
+    }
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  float2* ld = static_cast<float2*>(workspace);
+  if (d == 64)
+    return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ld, Nq_pad, s, dev);
+  return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ld, Nq_pad, s, dev);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d) {

@@ -1,0 +1,637 @@
+// Exact attention backward for sm_103a: dQ, dK, dV of
+// O = softmax(scale * Q K^T + causal mask) V, with the scores recomputed from
+// Q, K and the forward's row log-sum-exp instead of being stored ([MG-A] §3.3
+// says standard attention keeps the N x N matrix for the backward pass;
+// [MG-B] §3.2, engineering results: the tiled method recomputes it).
+//
+// The gradients are the chain rule through the forward definition:
+//   P = exp(S - lse), dV = P^T dO, dP = dO V^T, dS = P * (dP - Dl),
+//   Dl_i = sum_t dO_it O_it (equal to sum_j P_ij dP_ij), dQ = scale dS K,
+//   dK = scale dS^T Q; the query heads of a GQA group add into one dK, dV.
+//
+// Sources: [MG-A] menggq.pages.dev "Transformer 架构的数学与计算深度解析";
+// [MG-B] menggq.pages.dev "Transformer 深度进阶：从矩阵视角到 FlashAttention 工程优化".
+//
+// Three kernels, no atomics (the result is deterministic):
+//   bwd_prep_kernel      per query row: (lse * log2 e, Dl), each head padded to
+//                        a multiple of 128 rows with (+inf, 0) so that padded
+//                        rows get P = 0.
+//   attn_bwd_dkdv_kernel CTA = one 128-key tile of one (batch, KV head). It
+//                        streams every query tile of every query head of the
+//                        group; dK and dV accumulate in TMEM.
+//   attn_bwd_dq_kernel   CTA = one 128-row query tile; streams its key tiles;
+//                        dQ accumulates in TMEM.
+// Both main kernels: warps 0-7 elementwise (two warpgroups, each owning half
+// of the 128 columns of a score tile; thread = TMEM lane = row), warp 8 TMA
+// producer, warp 9 TMEM allocator + tcgen05.mma issuer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace attn_dev {
+
+struct BwdArgs {
+  __nv_bfloat16* dq;   // [B, Hq, Nq, D]
+  __nv_bfloat16* dk;   // [B, Hkv, Nk, D]
+  __nv_bfloat16* dv;   // [B, Hkv, Nk, D]
+  const float2* ld;    // [B * Hq][Nq_pad]: (lse * log2 e, Dl); padded rows (+inf, 0)
+  int B, Hq, Hkv, Nq, Nk, Nq_pad;
+  int group;           // Hq / Hkv
+  int causal;
+  int causal_offset;   // Nk - Nq: query i is aligned with key i + causal_offset
+  float scale;         // applied to dQ and dK in the epilogues
+  float scale_log2;    // scale * log2(e)
+  unsigned* status;
+};
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int KBLK = D / 64;
+  static constexpr int BLOCK_BYTES = 128 * 64 * 2;   // 128 rows x 64 columns, 128-byte swizzle
+  static constexpr int TILE_BYTES = KBLK * BLOCK_BYTES;
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int LD_BYTES = 128 * 8;           // (lse2, Dl) of 128 query rows
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+
+  // dK/dV kernel: K, V once; Q, dO and (lse2, Dl) per stage.
+  static constexpr int KV_K_OFF = 0;
+  static constexpr int KV_V_OFF = TILE_BYTES;
+  static constexpr int KV_Q_OFF = 2 * TILE_BYTES;
+  static constexpr int KV_DO_OFF = KV_Q_OFF + STAGES * TILE_BYTES;
+  static constexpr int KV_LD_OFF = KV_DO_OFF + STAGES * TILE_BYTES;
+  static constexpr int KV_BAR_OFF = KV_LD_OFF + STAGES * LD_BYTES;
+  // kv_full, full[S], empty[S], s_full, p_full[2], dv_done, dk_done, acc_done, drain
+  static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 7;
+  static constexpr int KV_MISC_OFF = KV_BAR_OFF + KV_NUM_BARS * 8;
+  static constexpr int KV_SMEM_BYTES = KV_MISC_OFF + 16 + 1024;
+  // TMEM columns: S^T, dP^T (128 each; P^T and dS^T are written back over
+  // them as packed bf16), then the dV and dK accumulators.
+  static constexpr uint32_t T_ST = 0, T_DPT = 128, T_DV = 256, T_DK = 256 + D;
+
+  // dQ kernel: Q, dO once; K, V per stage.
+  static constexpr int Q_Q_OFF = 0;
+  static constexpr int Q_DO_OFF = TILE_BYTES;
+  static constexpr int Q_K_OFF = 2 * TILE_BYTES;
+  static constexpr int Q_V_OFF = Q_K_OFF + STAGES * TILE_BYTES;
+  static constexpr int Q_BAR_OFF = Q_V_OFF + STAGES * TILE_BYTES;
+  // q_full, full[S], empty[S], s_full, p_full[2], dq_done, acc_done, drain
+  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 6;
+  static constexpr int Q_MISC_OFF = Q_BAR_OFF + Q_NUM_BARS * 8;
+  static constexpr int Q_SMEM_BYTES = Q_MISC_OFF + 16 + 1024;
+  // TMEM columns: two S buffers, dP (dS written back over it), dQ.
+  static constexpr uint32_t T_S0 = 0, T_DP = 128, T_DQ = 256, T_S1 = 384;
+};
+
+// Wait sites recorded in status[1] by the backward kernels.
+enum : unsigned {
+  kSiteBwdKvFull = 32, kSiteBwdEmpty, kSiteBwdFull, kSiteBwdDvDone, kSiteBwdDkDone, kSiteBwdPFull,
+  kSiteBwdSFull, kSiteBwdAccDone, kSiteBwdDrain, kSiteBwdLoadDrain, kSiteBwdQFull, kSiteBwdDqDone
+};
+
+// A of the P.V-shaped MMAs (P^T, dS^T or dS) sits in TMEM as packed bf16:
+// keys/queries 0-63 of the tile in columns [base, base + 32), 64-127 in
+// [base + 64, base + 96) (each warpgroup packs over the start of its own half).
+// K-step kk (16 values = 8 columns) therefore starts at this column.
+__device__ __forceinline__ uint32_t bwd_packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+// Per query row: lse2 = lse * log2(e) (+inf for a row that sees no key, so
+// that its P is 0) and Dl = sum_t dO_t O_t in fp32 over the bf16 inputs.
+// One 16-byte chunk per thread; the D/8 threads of a row reduce by shuffles.
+template <int D>
+__global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                const float* __restrict__ lse, float2* __restrict__ ld, long long heads, int Nq,
+                                int Nq_pad) {
+  constexpr int TPR = D / 8;
+  const long long n = heads * Nq_pad * TPR;
+  const long long stride = (long long)gridDim.x * blockDim.x;  // a multiple of 32
+  const int lane = threadIdx.x & 31;
+  for (long long base = (blockIdx.x * (long long)blockDim.x + threadIdx.x) - lane; base < n; base += stride) {
+    const long long e = base + lane;
+    const bool valid = e < n;
+    const long long row = e / TPR;
+    const int c = (int)(e % TPR);
+    const int i = (int)(row % Nq_pad);
+    const long long hh = row / Nq_pad;
+    float acc = 0.f;
+    if (valid && i < Nq) {
+      const size_t off = ((size_t)hh * Nq + i) * D + 8 * c;
+      const uint4 wo = *reinterpret_cast<const uint4*>(o + off);
+      const uint4 wd = *reinterpret_cast<const uint4*>(dout + off);
+      const uint32_t po[4] = {wo.x, wo.y, wo.z, wo.w}, pd[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(__uint_as_float(po[k] << 16), __uint_as_float(pd[k] << 16), acc);
+        acc = fmaf(__uint_as_float(po[k] & 0xffff0000u), __uint_as_float(pd[k] & 0xffff0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (valid && c == 0) {
+      float2 r = make_float2(CUDART_INF_F, 0.f);
+      if (i < Nq) {
+        const float l = lse[(size_t)hh * Nq + i];
+        r.x = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
+        r.y = acc;
+      }
+      ld[(size_t)hh * Nq_pad + i] = r;
+    }
+  }
+}
+
+// Shared epilogue: 32 fp32 columns of the thread's TMEM lane, times `mul`,
+// rounded to bf16 and stored to dst (or zeros when there is no accumulator).
+__device__ __forceinline__ void bwd_store32(uint32_t taddr, bool have, float mul, __nv_bfloat16* dst, bool store) {
+  uint32_t r[32];
+  if (have) {
+    tmem_ld32(taddr, r);
+    tmem_wait_ld();
+    tmem_reg_fence(r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = 0u;
+  }
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+  if (store) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+}
+
+// ============================================================== dK, dV
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + C::KV_K_OFF;
+  uint8_t* sV = smem + C::KV_V_OFF;
+  uint8_t* sQ = smem + C::KV_Q_OFF;
+  uint8_t* sDO = smem + C::KV_DO_OFF;
+  uint8_t* sLD = smem + C::KV_LD_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::KV_BAR_OFF);
+  uint64_t* kv_full = bars;
+  uint64_t* full = bars + 1;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* s_full = empty + C::STAGES;
+  uint64_t* p_full = s_full + 1;  // [2], one per warpgroup
+  uint64_t* dv_done = p_full + 2;
+  uint64_t* dk_done = dv_done + 1;
+  uint64_t* acc_done = dk_done + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::KV_MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::KV_MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int hkv = blockIdx.x;
+  const int kt = blockIdx.y;  // key tile 0 (most query tiles under causal masking) launches first
+  const int b = blockIdx.z;
+  const int key0 = kt * 128;
+  // Query tiles holding a row that sees some key of this tile: [qt0, n_qt).
+  const int n_qt = (a.Nq + 127) / 128;
+  int qt0 = 0;
+  if (a.causal) {
+    const long long first = (long long)key0 - a.causal_offset;  // first query row that sees key0
+    qt0 = first <= 0 ? 0 : (int)min((long long)n_qt, first / 128);
+  }
+  const int per_head = n_qt - qt0;
+  const int n_steps = per_head * a.group;  // step n: head hkv*group + n / per_head, tile qt0 + n % per_head
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(p_full + 1, 128);
+    mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_steps > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      for (int kb = 0; kb < C::KBLK; ++kb) {
+        tma_load_3d(sK + kb * C::BLOCK_BYTES, &tm_k, kv_full, kb * 64, key0, b * a.Hkv + hkv);
+        tma_load_3d(sV + kb * C::BLOCK_BYTES, &tm_v, kv_full, kb * 64, key0, b * a.Hkv + hkv);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_steps; ++n) {
+        const int s = n % C::STAGES, u = n / C::STAGES;
+        if (u > 0 && !mbar_wait(empty + s, (u - 1) & 1, a.status, kSiteBwdEmpty)) { *abort_flag = 1; break; }
+        const int h = hkv * a.group + n / per_head;
+        const int q0 = (qt0 + n % per_head) * 128;
+        mbar_arrive_expect_tx(full + s, 2 * C::TILE_BYTES + C::LD_BYTES);
+        for (int kb = 0; kb < C::KBLK; ++kb) {
+          tma_load_3d(sQ + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, full + s, kb * 64, q0, b * a.Hq + h);
+          tma_load_3d(sDO + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_do, full + s, kb * 64, q0, b * a.Hq + h);
+        }
+        bulk_load(sLD + s * C::LD_BYTES, a.ld + (size_t)(b * a.Hq + h) * a.Nq_pad + q0, C::LD_BYTES, full + s);
+        issued = n + 1;
+        if (*abort_flag) break;
+      }
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA exits.
+        mbar_wait(kv_full, 0, a.status, kSiteBwdLoadDrain);
+        for (int n = max(0, issued - C::STAGES); n < issued; ++n)
+          mbar_wait(full + n % C::STAGES, (n / C::STAGES) & 1, a.status, kSiteBwdLoadDrain);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      bool ok = mbar_wait(kv_full, 0, a.status, kSiteBwdKvFull);
+      for (int n = 0; ok && n < n_steps; ++n) {
+        const int s = n % C::STAGES;
+        if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
+        const uint32_t q_addr = smem_u32(sQ + s * C::TILE_BYTES);
+        const uint32_t do_addr = smem_u32(sDO + s * C::TILE_BYTES);
+        // S^T overwrites P^T of the previous step (read by its dV MMAs).
+        if (n > 0 && !(ok = mbar_wait(dv_done, (n - 1) & 1, a.status, kSiteBwdDvDone))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+          umma_ss(tmem + C::T_ST, smem_desc_sw128(k_addr + off, 16, 1024), smem_desc_sw128(q_addr + off, 16, 1024),
+                  idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        // dP^T overwrites dS^T of the previous step (read by its dK MMAs).
+        if (n > 0 && !(ok = mbar_wait(dk_done, (n - 1) & 1, a.status, kSiteBwdDkDone))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+          umma_ss(tmem + C::T_DPT, smem_desc_sw128(v_addr + off, 16, 1024),
+                  smem_desc_sw128(do_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        // dV += P^T dO and dK += dS^T Q, one half of the query columns per
+        // warpgroup as soon as that warpgroup has written it.
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+            umma_ts(tmem + C::T_DV, tmem + C::T_ST + bwd_packed_col(kk),
+                    smem_desc_sw128(do_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
+                    (n > 0 || kk > 0) ? 1u : 0u);
+          if (g == 1) umma_commit(dv_done);
+#pragma unroll
+          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+            umma_ts(tmem + C::T_DK, tmem + C::T_DPT + bwd_packed_col(kk),
+                    smem_desc_sw128(q_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
+                    (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        umma_commit(dk_done);
+        umma_commit(empty + s);
+      }
+      if (!ok) *abort_flag = 1;
+      umma_commit(acc_done);
+      // Every MMA issued above has finished before TMEM is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.status, kSiteBwdDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups
+    const int g = warp >> 2;  // query columns [64g, 64g + 64) of every tile
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row in the tile
+    const int kj = key0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int n = 0; ok && n < n_steps; ++n) {
+      const int s = n % C::STAGES;
+      const int q0 = (qt0 + n % per_head) * 128;
+      if (!(ok = mbar_wait(s_full, n & 1, a.status, kSiteBwdSFull))) break;
+      // (lse2, Dl) of this stage arrived by bulk copy: observe its barrier
+      // here too (already complete) so the copy's writes are visible.
+      if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
+      tc_fence_after_sync();
+      const float4* ldp = reinterpret_cast<const float4*>(sLD + s * C::LD_BYTES) + 32 * g;
+      // query q0 + 64g + c sees key kj iff c >= kj - causal_offset - q0 - 64g
+      const bool need_mask = a.causal && key0 + 127 > q0 + 64 * g + a.causal_offset;
+      const int cmin = kj - a.causal_offset - q0 - 64 * g;
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_off + C::T_ST + 64 * g + 32 * pass, sr);
+        tmem_ld32(tmem + lane_off + C::T_DPT + 64 * g + 32 * pass, dr);
+        tmem_wait_ld();
+        tmem_reg_fence(sr);
+        tmem_reg_fence(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * pass + 2 * i;
+          const float4 L = ldp[16 * pass + i];  // (lse2_c, Dl_c, lse2_c+1, Dl_c+1), same for the whole warp
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -L.x, -L.z);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (need_mask) {
+            p0 = c < cmin ? 0.f : p0;
+            p1 = c + 1 < cmin ? 0.f : p1;
+          }
+          const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - L.y);
+          const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - L.w);
+          pk[i] = pack_bf16x2(p0, p1);
+          dk[i] = pack_bf16x2(ds0, ds1);
+        }
+        // Packed over columns this warpgroup has already read.
+        tmem_st16(tmem + lane_off + C::T_ST + 64 * g + 16 * pass, pk);
+        tmem_st16(tmem + lane_off + C::T_DPT + 64 * g + 16 * pass, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(p_full + g);
+    }
+    if (!ok) *abort_flag = 1;
+    // ---------------------------------------------------------- epilogue
+    bool have = false;
+    if (ok && n_steps > 0) {
+      have = ok = mbar_wait(acc_done, 0, a.status, kSiteBwdAccDone);
+      tc_fence_after_sync();
+      if (*abort_flag) have = false;
+    }
+    // warpgroup 0 writes dV, warpgroup 1 writes dK (times the score scale)
+    const bool in_range = kj < a.Nk;
+    __nv_bfloat16* dst = (g == 0 ? a.dv : a.dk) + ((size_t)(b * a.Hkv + hkv) * a.Nk + (in_range ? kj : 0)) * D;
+    const uint32_t col = g == 0 ? C::T_DV : C::T_DK;
+    const float mul = g == 0 ? 1.f : a.scale;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) bwd_store32(tmem + lane_off + col + 32 * c, have, mul, dst + 32 * c, in_range);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ============================================================== dQ
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::Q_Q_OFF;
+  uint8_t* sDO = smem + C::Q_DO_OFF;
+  uint8_t* sK = smem + C::Q_K_OFF;
+  uint8_t* sV = smem + C::Q_V_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* full = bars + 1;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* s_full = empty + C::STAGES;
+  uint64_t* p_full = s_full + 1;  // [2]
+  uint64_t* dq_done = p_full + 2;
+  uint64_t* acc_done = dq_done + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::Q_MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::Q_MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int n_qt = (a.Nq + 127) / 128;
+  const int qt = n_qt - 1 - blockIdx.y;  // latest (most key tiles under causal masking) first
+  const int b = blockIdx.z;
+  const int hkv = h / a.group;
+  const int q0 = qt * 128;
+  // Key tiles [0, n_kt): up to the last key the tile's last row sees.
+  const int last = min(q0 + 127, a.Nq - 1);
+  const long long hi = a.causal ? min((long long)a.Nk - 1, (long long)last + a.causal_offset) : a.Nk - 1;
+  const int n_kt = hi >= 0 ? (int)(hi / 128) + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(p_full + 1, 128);
+    mbar_init(dq_done, 1);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+      for (int kb = 0; kb < C::KBLK; ++kb) {
+        tma_load_3d(sQ + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q0, b * a.Hq + h);
+        tma_load_3d(sDO + kb * C::BLOCK_BYTES, &tm_do, q_full, kb * 64, q0, b * a.Hq + h);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_kt; ++n) {
+        const int s = n % C::STAGES, u = n / C::STAGES;
+        if (u > 0 && !mbar_wait(empty + s, (u - 1) & 1, a.status, kSiteBwdEmpty)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(full + s, 2 * C::TILE_BYTES);
+        for (int kb = 0; kb < C::KBLK; ++kb) {
+          tma_load_3d(sK + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_k, full + s, kb * 64, n * 128,
+                      b * a.Hkv + hkv);
+          tma_load_3d(sV + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_v, full + s, kb * 64, n * 128,
+                      b * a.Hkv + hkv);
+        }
+        issued = n + 1;
+        if (*abort_flag) break;
+      }
+      if (*abort_flag) {
+        mbar_wait(q_full, 0, a.status, kSiteBwdLoadDrain);
+        for (int n = max(0, issued - C::STAGES); n < issued; ++n)
+          mbar_wait(full + n % C::STAGES, (n / C::STAGES) & 1, a.status, kSiteBwdLoadDrain);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kt > 0) {
+      constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+      auto issue_s = [&](int n) {  // S(n) = Q K_n^T into S buffer n & 1
+        const uint32_t k_addr = smem_u32(sK + (n % C::STAGES) * C::TILE_BYTES);
+        const uint32_t dst = tmem + ((n & 1) ? C::T_S1 : C::T_S0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+          umma_ss(dst, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024), idesc_ss,
+                  kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, a.status, kSiteBwdQFull) && mbar_wait(full, 0, a.status, kSiteBwdFull);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0);
+      }
+      for (int n = 0; ok && n < n_kt; ++n) {
+        const int s = n % C::STAGES;
+        // dP overwrites dS of the previous step (read by its dQ MMAs).
+        if (n > 0 && !(ok = mbar_wait(dq_done, (n - 1) & 1, a.status, kSiteBwdDqDone))) break;
+        tc_fence_after_sync();
+        const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+          umma_ss(tmem + C::T_DP, smem_desc_sw128(do_addr + off, 16, 1024), smem_desc_sw128(v_addr + off, 16, 1024),
+                  idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);  // S(n) and dP(n)
+        // S(n+1) into the other buffer (its previous contents, S(n-1), were
+        // read before the elementwise warps signalled step n-1) while the
+        // elementwise warps work on step n.
+        if (n + 1 < n_kt) {
+          if (!(ok = mbar_wait(full + (n + 1) % C::STAGES, ((n + 1) / C::STAGES) & 1, a.status, kSiteBwdFull)))
+            break;
+          tc_fence_after_sync();
+          issue_s(n + 1);
+        }
+        const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+            umma_ts(tmem + C::T_DQ, tmem + C::T_DP + bwd_packed_col(kk),
+                    smem_desc_sw128(k_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
+                    (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        umma_commit(dq_done);
+        umma_commit(empty + s);
+      }
+      if (!ok) *abort_flag = 1;
+      umma_commit(acc_done);
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.status, kSiteBwdDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups
+    const int g = warp >> 2;  // key columns [64g, 64g + 64) of every tile
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int qi = q0 + r;  // < Nq_pad
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const float2 L = a.ld[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
+    const float lse2 = L.x, dl = L.y;
+    // last key this row sees (keys past it are masked)
+    const long long lim_ll = a.causal ? min((long long)a.Nk - 1, (long long)qi + a.causal_offset) : a.Nk - 1;
+    const int lim = (int)max(lim_ll, -1LL);
+    // the tile needs masking when a row's limit falls inside it (tile-uniform test on the first row)
+    const long long lim_first = a.causal ? min((long long)a.Nk - 1, (long long)q0 + a.causal_offset) : a.Nk - 1;
+    bool ok = true;
+    for (int n = 0; ok && n < n_kt; ++n) {
+      if (!(ok = mbar_wait(s_full, n & 1, a.status, kSiteBwdSFull))) break;
+      tc_fence_after_sync();
+      const uint32_t tS = tmem + lane_off + ((n & 1) ? C::T_S1 : C::T_S0) + 64 * g;
+      const int kbase = n * 128 + 64 * g;
+      const bool need_mask = kbase + 63 > lim_first;
+      const int cmax = lim - kbase;  // column c is visible iff c <= cmax
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + 32 * pass, sr);
+        tmem_ld32(tmem + lane_off + C::T_DP + 64 * g + 32 * pass, dr);
+        tmem_wait_ld();
+        tmem_reg_fence(sr);
+        tmem_reg_fence(dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * pass + 2 * i;
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -lse2, -lse2);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (need_mask) {
+            p0 = c > cmax ? 0.f : p0;
+            p1 = c + 1 > cmax ? 0.f : p1;
+          }
+          dk[i] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * i]) - dl), p1 * (__uint_as_float(dr[2 * i + 1]) - dl));
+        }
+        tmem_st16(tmem + lane_off + C::T_DP + 64 * g + 16 * pass, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(p_full + g);
+    }
+    if (!ok) *abort_flag = 1;
+    // ---------------------------------------------------------- epilogue
+    bool have = false;
+    if (ok && n_kt > 0) {
+      have = ok = mbar_wait(acc_done, 0, a.status, kSiteBwdAccDone);
+      tc_fence_after_sync();
+      if (*abort_flag) have = false;
+    }
+    const bool in_range = qi < a.Nq;
+    __nv_bfloat16* dst = a.dq + ((size_t)(b * a.Hq + h) * a.Nq + (in_range ? qi : 0)) * D;
+    // warpgroup g writes columns [g D/2, (g+1) D/2)
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      const int col = g * (D / 2) + 32 * c;
+      bwd_store32(tmem + lane_off + C::T_DQ + col, have, a.scale, dst + col, in_range);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace attn_dev

@@ -108,6 +108,17 @@ def prefill_inputs(w: Prefill):
     return q, k, v
 
 
+def backward_inputs(w: Prefill):
+    """(q, k, v, dout) as contiguous CPU bf16 tensors: the prefill draw (Q, K, V),
+    then dO = dL/dO from the same generator, all N(0, 1) rounded to bf16."""
+    gen = torch.Generator().manual_seed(w.seed)
+    q = _randn_bf16(gen, (w.B, w.Hq, w.Nq, w.d))
+    k = _randn_bf16(gen, (w.B, w.Hkv, w.Nk, w.d))
+    v = _randn_bf16(gen, (w.B, w.Hkv, w.Nk, w.d))
+    dout = _randn_bf16(gen, (w.B, w.Hq, w.Nq, w.d))
+    return q, k, v, dout
+
+
 def decode_inputs(w: Decode):
     """(q, k_cache, v_cache, seqlens): lengths first, then q, K cache, V cache."""
     gen = torch.Generator().manual_seed(w.seed)

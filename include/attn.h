@@ -99,7 +99,8 @@ ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v
 
 /*
  * Workspace bytes attn_fwd_rope needs: the rotated K ([B, Hkv, Nk, d] bf16)
- * and a (cos, sin) table of max(Nk, Nq) positions x d/2 pairs (fp32).
+ * and two layouts (position-major, pair-major) of a (cos, sin) table of
+ * max(Nk, Nq) positions x d/2 pairs (fp32).
  * 0 for arguments attn_fwd_rope would reject.
  */
 ATTN_API size_t attn_fwd_rope_workspace_size(int B, int Hkv, int Nq, int Nk, int d);
@@ -122,6 +123,38 @@ ATTN_API size_t attn_fwd_rope_workspace_size(int B, int Hkv, int Nq, int Nk, int
 ATTN_API attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                                    int Hkv, int Nq, int Nk, int d, float scale, int causal, int window,
                                    float rope_base, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes attn_bwd needs: 8 bytes per query row, each head's rows
+ * padded to a multiple of 128. 0 for arguments attn_bwd would reject.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
+
+/*
+ * Backward pass of attn_fwd (causal or not, MHA/GQA/MQA): given the forward's
+ * inputs, its output o and row LSE, and dout = dL/dO, writes dq = dL/dQ,
+ * dk = dL/dK and dv = dL/dV. The scores are recomputed from q, k and lse
+ * instead of being stored ([MG-A] §3.3; [MG-B] §3.2): with P = softmax(scale
+ * Q K^T + mask), dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)),
+ * dQ = scale dS K, dK = scale dS^T Q; the query heads of a GQA group add
+ * into their shared dK, dV. No atomics: the result is deterministic.
+ *
+ *   q, dout, o  [B, Hq, Nq, d] bf16 (device); o as written by attn_fwd
+ *   k, v        [B, Hkv, Nk, d] bf16 (device)
+ *   lse         [B, Hq, Nq] fp32 (device), natural log, as written by
+ *               attn_fwd (-inf for a row that sees no key); required
+ *   dq          [B, Hq, Nq, d] bf16 (device, written)
+ *   dk, dv      [B, Hkv, Nk, d] bf16 (device, written)
+ *   workspace   >= attn_bwd_workspace_size(B, Hq, Nq) bytes, 256-byte
+ *               aligned, contents irrelevant (overwritten)
+ * Rows of dq that see no key are 0; keys no query sees get dk = dv = 0.
+ * scale, causal (bottom-right aligned when Nq != Nk), d and the alignment
+ * rules as attn_fwd. Three kernels run on `stream` in order: a per-row
+ * prologue, then dK/dV, then dQ.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                              int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Size in bytes of the device workspace attn_decode needs for these sizes

@@ -102,7 +102,8 @@ def attention_forward(q, k, v, scale: float, causal: bool, rows=None, row_block:
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_rows=None, row_block: int = 1024):
+def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_rows=None, row_block: int = 1024,
+                       magnitudes: bool = False):
     """Gradients of O = softmax(scale * Q K^T + mask) V with respect to Q, K, V.
 
     Given dO = dL/dO for some loss L, returns (dq, dk, dv) = dL/dQ, dL/dK,
@@ -128,6 +129,19 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_r
     select which query rows of dq and which key rows of dk, dv are returned
     (all by default); every query row's full score vector is still
     materialised, in blocks of ``row_block`` rows, before its softmax.
+
+    magnitudes=True returns (dq, dk, dv, mags), mags holding the scales that
+    rounding errors of an implementation are measured against (test use):
+      tq, tk, tv  per element, the sum of the absolute values of the terms it
+                  adds up (scale |dS| |K|, scale |dS|^T |Q|, P^T |dO|); a sum
+                  of large cancelling terms can be much smaller than this.
+      sq, sk      how far dq, dk move when Dl is formed from an O whose
+                  components carry relative errors of size one (first order):
+                  with e_it = sqrt(sum_j P_ij^2 v_jt^2) + |O_it| (the size of
+                  O_it and of the spread of its terms), Dl_i moves by about
+                  r_i = sqrt(sum_t dO_it^2 e_it^2), so dq_it by
+                  scale r_i sum_j P_ij |k_jt| and dk_jt by
+                  scale sum_i P_ij r_i |q_it|.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -141,6 +155,8 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_r
     dq = np.zeros((B, Hq, q_rows.size, d))
     dk = np.zeros((B, Hkv, k_rows.size, d))
     dv = np.zeros((B, Hkv, k_rows.size, dv_))
+    tq, tk, tv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
+    sq, sk = np.zeros_like(dq), np.zeros_like(dk)
     keys = np.arange(Nk)
     want_q = np.zeros(Nq, dtype=bool)
     want_q[q_rows] = True
@@ -160,12 +176,24 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, q_rows=None, k_r
                 P, _ = _two_pass_softmax(S)
                 dP = do[b, h, ri] @ vh.T
                 dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                if magnitudes:
+                    e = np.sqrt((P ** 2) @ (vh ** 2)) + np.abs(P @ vh)
+                    r = np.sqrt(((do[b, h, ri] * e) ** 2).sum(axis=1))
                 sel = want_q[ri]
                 if sel.any():
                     dq[b, h, q_pos[ri[sel]]] = scale * (dS[sel] @ kh)
+                    if magnitudes:
+                        tq[b, h, q_pos[ri[sel]]] = scale * (np.abs(dS[sel]) @ np.abs(kh))
+                        sq[b, h, q_pos[ri[sel]]] = scale * r[sel, None] * (P[sel] @ np.abs(kh))
                 if k_rows.size:
                     dv[b, g] += P[:, k_rows].T @ do[b, h, ri]
                     dk[b, g] += scale * (dS[:, k_rows].T @ q[b, h, ri])
+                    if magnitudes:
+                        tv[b, g] += P[:, k_rows].T @ np.abs(do[b, h, ri])
+                        tk[b, g] += scale * (np.abs(dS[:, k_rows]).T @ np.abs(q[b, h, ri]))
+                        sk[b, g] += scale * ((P[:, k_rows] * r[:, None]).T @ np.abs(q[b, h, ri]))
+    if magnitudes:
+        return dq, dk, dv, {"tq": tq, "tk": tk, "tv": tv, "sq": sq, "sk": sk}
     return dq, dk, dv
 
 

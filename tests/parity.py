@@ -4,6 +4,21 @@ The bar (one set of numbers for every case): compared against the fp64
 oracle on the same bf16 inputs, the bf16 output must have max-abs error
 <= 1e-2 and mean-abs error <= 1e-3, and the fp32 LSE max-abs error <= 1e-3.
 Rows the oracle marks as seeing no key must come back as o = 0, lse = -inf.
+
+Gradients (dQ, dK, dV) have no stated bar; the one used is derived from the
+arithmetic of the backward path, with u = 2^-8 the unit roundoff of bf16.
+Each gradient element g is a sum of terms in which one factor (P or dS) was
+rounded to bf16 (error <= u |term|), Dl comes from the bf16 forward output
+(an error of the same order), and g is rounded to bf16 (<= u |g|). With T the
+sum of the terms' absolute values (the oracle returns it: a sum of large
+cancelling terms, e.g. a causal row that sees few keys, can be much smaller
+than T) and S the oracle's first-order sensitivity of g to errors of relative
+size one in the components of O (Dl = sum_t dO_t O_t uses the bf16 forward
+output, whose components are off by about u; S is 0 for dV), every element
+must satisfy
+    |g - g_ref| <= 4u (T + S) + u |g_ref| + 2^-16
+(2^-16 covers the fp32 accumulation residue where T and S vanish), and over
+a tensor mean |g - g_ref| <= u mean(T + S).
 """
 import numpy as np
 import torch
@@ -14,6 +29,9 @@ from exact_scaled_dot_03_b300.workloads import bf16_bits
 O_MAX_ABS = 1e-2
 O_MEAN_ABS = 1e-3
 LSE_MAX_ABS = 1e-3
+BF16_U = 2.0 ** -8
+GRAD_TERMS = 4 * BF16_U
+GRAD_FLOOR = 2.0 ** -16
 
 
 def f64(t: torch.Tensor) -> np.ndarray:
@@ -41,4 +59,23 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
         lerr = np.abs(lse[~empty] - lse_ref[~empty])
         res["lse_max_abs"] = float(lerr.max()) if lerr.size else 0.0
         assert res["lse_max_abs"] <= LSE_MAX_ABS, f"{what}: {res}"
+    return res
+
+
+def compare_grad(g_gpu, g_ref, t_ref, s_ref=None, what=""):
+    """Assert the gradient bar (module docstring) given the oracle's gradient
+    g_ref, its term magnitudes t_ref and its Dl sensitivity s_ref (None for
+    dV); returns the measured errors."""
+    g = f64(g_gpu)
+    assert g.shape == g_ref.shape == t_ref.shape, f"{what}: shape {g.shape} vs {g_ref.shape}"
+    assert np.isfinite(g).all(), f"{what}: non-finite gradient"
+    if g.size == 0:
+        return {}
+    scale = t_ref if s_ref is None else t_ref + s_ref
+    err = np.abs(g - g_ref)
+    bound = GRAD_TERMS * scale + BF16_U * np.abs(g_ref) + GRAD_FLOOR
+    res = {"max_abs": float(err.max()), "worst_of_bound": float((err / bound).max()),
+           "mean_abs": float(err.mean()), "mean_of_bound": float(err.mean() / max(BF16_U * scale.mean(), GRAD_FLOOR))}
+    assert res["worst_of_bound"] <= 1.0, f"{what}: {res}"
+    assert res["mean_of_bound"] <= 1.0, f"{what}: {res}"
     return res

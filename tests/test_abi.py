@@ -161,6 +161,28 @@ def test_fwd_rope_argument_checks(lib):
     assert lib.attn_fwd_rope_workspace_size(1, 1, 20, 16, 64) == 2048 + 2 * 20 * 32 * 8  # queries before key 0
 
 
+def test_bwd_argument_checks(lib):
+    f = lambda **kw: lib.attn_bwd(*[kw.get(n, dflt) for n, dflt in [
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("o", FAKE), ("lse", FAKE), ("do", FAKE), ("dq", FAKE),
+        ("dk", FAKE), ("dv", FAKE), ("B", 1), ("Hq", 4), ("Hkv", 2), ("Nq", 200), ("Nk", 300), ("d", 128),
+        ("scale", 0.088), ("causal", 1), ("ws", 0x100000), ("wsb", 1 << 30), ("stream", None)]])
+    assert f(lse=None) == binding.ERR_INVALID_ARG         # the forward's LSE is required
+    assert f(do=None) == binding.ERR_INVALID_ARG
+    assert f(dk=None) == binding.ERR_INVALID_ARG
+    assert f(Hq=3) == binding.ERR_INVALID_ARG             # Hq % Hkv != 0
+    assert f(causal=2) == binding.ERR_INVALID_ARG
+    assert f(scale=0.0) == binding.ERR_INVALID_ARG
+    assert f(dq=FAKE + 8) == binding.ERR_INVALID_ARG      # not 16-byte aligned
+    assert f(ws=0x100010) == binding.ERR_INVALID_ARG      # not 256-byte aligned
+    assert f(ws=None) == binding.ERR_INVALID_ARG
+    assert f(wsb=4 * 256 * 8 - 1) == binding.ERR_INVALID_ARG
+    assert f(d=96) == binding.ERR_UNSUPPORTED
+    # (lse2, Dl) per query row, each head padded to 128 rows
+    assert lib.attn_bwd_workspace_size(1, 4, 200) == 4 * 256 * 8
+    assert lib.attn_bwd_workspace_size(2, 3, 128) == 6 * 128 * 8
+    assert lib.attn_bwd_workspace_size(0, 4, 200) == 0
+
+
 def test_paged_workspace_size(lib):
     # same plan as the contiguous decode with Lmax = pages * page_size
     assert binding.lib().attn_decode_paged_workspace_size(16, 32, 8, 128, 64, 128) == \

@@ -651,3 +651,39 @@ def test_sum_invariant_catches_a_dropped_softmax_correction():
     assert np.abs(wrong_dk.sum(axis=0)).max() > 1e-3
     _, dk, _ = attention_backward(q, k, v, do, 0.5, False)
     assert np.abs(dk[0, 0].sum(axis=0)).max() < 1e-12
+
+
+def test_backward_term_magnitudes():
+    """The magnitude sums bound the gradients (triangle inequality), equal them
+    where every term is non-negative, and do not change the gradients; the
+    Dl sensitivities bound the first-order move of dq, dk when O's
+    components are perturbed by at most e_it relatively."""
+    rng = np.random.default_rng(46)
+    q, k, v = _rand(rng, 1, 4, 21, 8), _rand(rng, 1, 2, 21, 8), _rand(rng, 1, 2, 21, 8)
+    do = _rand(rng, 1, 4, 21, 8)
+    plain = attention_backward(q, k, v, do, 0.4, True)
+    dq, dk, dv, m = attention_backward(q, k, v, do, 0.4, True, magnitudes=True)
+    for a, b_ in zip(plain, (dq, dk, dv)):
+        np.testing.assert_array_equal(a, b_)
+    for g, t in ((dq, m["tq"]), (dk, m["tk"]), (dv, m["tv"])):
+        assert (t >= np.abs(g) - 1e-12).all()
+    _, _, dv_pos, m_pos = attention_backward(q, k, v, np.abs(do), 0.4, True, magnitudes=True)
+    np.testing.assert_allclose(m_pos["tv"], dv_pos, atol=1e-12)   # P >= 0 and dO >= 0: no cancellation
+    # one key per row: dS = 0, so dq has no terms; Dl still moves dq
+    _, _, _, m1 = attention_backward(q, k[:, :, :1], v[:, :, :1], do, 0.4, False, magnitudes=True)
+    np.testing.assert_allclose(m1["tq"], 0.0, atol=1e-12)
+    assert (m1["sq"] > 0).all()
+    # dO = 0: nothing moves
+    _, _, _, m0 = attention_backward(q, k, v, np.zeros_like(do), 0.4, True, magnitudes=True)
+    assert np.abs(m0["sq"]).max() == 0 and np.abs(m0["sk"]).max() == 0
+    # brute force for one row: perturbing Dl by its bound r moves dq by at most sq
+    B, H, N, d = 1, 1, 6, 4
+    q1, k1, v1, do1 = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d), _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    S = 0.5 * q1[0, 0] @ k1[0, 0].T
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    e = np.sqrt((P ** 2) @ (v1[0, 0] ** 2)) + np.abs(P @ v1[0, 0])
+    r = np.sqrt(((do1[0, 0] * e) ** 2).sum(axis=1))
+    moved = 0.5 * (P * r[:, None]) @ k1[0, 0]            # dq change for Dl -> Dl - r
+    _, _, _, mm = attention_backward(q1, k1, v1, do1, 0.5, False, magnitudes=True)
+    assert (np.abs(moved) <= mm["sq"][0, 0] + 1e-12).all()
