@@ -22,8 +22,14 @@
 //   attn_bwd_dq_kernel   CTA = one 128-row query tile; streams its key tiles;
 //                        dQ accumulates in TMEM.
 // Both main kernels: warps 0-7 elementwise (two warpgroups, each owning half
-// of the 128 columns of a score tile; thread = TMEM lane = row), warp 8 TMA
-// producer, warp 9 TMEM allocator + tcgen05.mma issuer.
+// g of the 128 columns of a score tile; thread = TMEM lane = row), warp 8 TMA
+// producer, warp 9 TMEM allocator + tcgen05.mma issuer. The elementwise work
+// of a step runs in two phases, P = exp2(S - lse) (the exponentials) as soon
+// as S is in TMEM and dS = P (dP - Dl) once dP is, so each phase overlaps a
+// different MMA group (all MMAs are M = N = 128):
+//   dK/dV step: S^T | dP^T (P phase) | dV (dS phase) | dK
+//   dQ step:    dP(n) (P phase) | S(n+1) (dS phase) | dQ(n)
+// (S double-buffered in the dQ kernel so the next one is already queued).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -65,8 +71,8 @@ struct BwdCfg {
   static constexpr int KV_DO_OFF = KV_Q_OFF + STAGES * TILE_BYTES;
   static constexpr int KV_LD_OFF = KV_DO_OFF + STAGES * TILE_BYTES;
   static constexpr int KV_BAR_OFF = KV_LD_OFF + STAGES * LD_BYTES;
-  // kv_full, full[S], empty[S], s_full, p_full[2], dv_done, dk_done, acc_done, drain
-  static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 7;
+  // kv_full, full[S], empty[S], s_full, dp_full, p_full[2], ds_full[2], dv_done, dk_done, acc_done, drain
+  static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 10;
   static constexpr int KV_MISC_OFF = KV_BAR_OFF + KV_NUM_BARS * 8;
   static constexpr int KV_SMEM_BYTES = KV_MISC_OFF + 16 + 1024;
   // TMEM columns: S^T, dP^T (128 each; P^T and dS^T are written back over
@@ -79,18 +85,19 @@ struct BwdCfg {
   static constexpr int Q_K_OFF = 2 * TILE_BYTES;
   static constexpr int Q_V_OFF = Q_K_OFF + STAGES * TILE_BYTES;
   static constexpr int Q_BAR_OFF = Q_V_OFF + STAGES * TILE_BYTES;
-  // q_full, full[S], empty[S], s_full, p_full[2], dq_done, acc_done, drain
-  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 6;
+  // q_full, full[S], empty[S], s_full[2] (one per S buffer), dp_full, ds_full[2], dq_done, acc_done, drain
+  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 9;
   static constexpr int Q_MISC_OFF = Q_BAR_OFF + Q_NUM_BARS * 8;
   static constexpr int Q_SMEM_BYTES = Q_MISC_OFF + 16 + 1024;
-  // TMEM columns: two S buffers, dP (dS written back over it), dQ.
+  // TMEM columns: S buffer 0, dP (dS written back over it), dQ, S buffer 1.
   static constexpr uint32_t T_S0 = 0, T_DP = 128, T_DQ = 256, T_S1 = 384;
 };
 
 // Wait sites recorded in status[1] by the backward kernels.
 enum : unsigned {
   kSiteBwdKvFull = 32, kSiteBwdEmpty, kSiteBwdFull, kSiteBwdDvDone, kSiteBwdDkDone, kSiteBwdPFull,
-  kSiteBwdSFull, kSiteBwdAccDone, kSiteBwdDrain, kSiteBwdLoadDrain, kSiteBwdQFull, kSiteBwdDqDone
+  kSiteBwdSFull, kSiteBwdAccDone, kSiteBwdDrain, kSiteBwdLoadDrain, kSiteBwdQFull, kSiteBwdDqDone,
+  kSiteBwdDpFull, kSiteBwdDsFull
 };
 
 // A of the P.V-shaped MMAs (P^T, dS^T or dS) sits in TMEM as packed bf16:
@@ -183,9 +190,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = bars;
   uint64_t* full = bars + 1;
   uint64_t* empty = full + C::STAGES;
-  uint64_t* s_full = empty + C::STAGES;
-  uint64_t* p_full = s_full + 1;  // [2], one per warpgroup
-  uint64_t* dv_done = p_full + 2;
+  uint64_t* s_full = empty + C::STAGES;  // S^T in TMEM
+  uint64_t* dp_full = s_full + 1;        // dP^T in TMEM
+  uint64_t* p_full = dp_full + 1;        // [2] warpgroup g wrote P^T of its half
+  uint64_t* ds_full = p_full + 2;        // [2] warpgroup g wrote dS^T of its half
+  uint64_t* dv_done = ds_full + 2;
   uint64_t* dk_done = dv_done + 1;
   uint64_t* acc_done = dk_done + 1;
   uint64_t* drain = acc_done + 1;
@@ -215,8 +224,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(p_full + 1, 128);
+    mbar_init(dp_full, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(p_full + g, 128);
+      mbar_init(ds_full + g, 128);
+    }
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
         const uint32_t q_addr = smem_u32(sQ + s * C::TILE_BYTES);
         const uint32_t do_addr = smem_u32(sDO + s * C::TILE_BYTES);
-        // S^T overwrites P^T of the previous step (read by its dV MMAs).
+        // S^T = K Q^T overwrites P^T of the previous step (read by its dV MMAs).
         if (n > 0 && !(ok = mbar_wait(dv_done, (n - 1) & 1, a.status, kSiteBwdDvDone))) break;
         tc_fence_after_sync();
 #pragma unroll
@@ -286,7 +298,8 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss(tmem + C::T_ST, smem_desc_sw128(k_addr + off, 16, 1024), smem_desc_sw128(q_addr + off, 16, 1024),
                   idesc_ss, kk > 0 ? 1u : 0u);
         }
-        // dP^T overwrites dS^T of the previous step (read by its dK MMAs).
+        umma_commit(s_full);
+        // dP^T = V dO^T overwrites dS^T of the previous step (read by its dK MMAs).
         if (n > 0 && !(ok = mbar_wait(dk_done, (n - 1) & 1, a.status, kSiteBwdDkDone))) break;
         tc_fence_after_sync();
 #pragma unroll
@@ -295,9 +308,8 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss(tmem + C::T_DPT, smem_desc_sw128(v_addr + off, 16, 1024),
                   smem_desc_sw128(do_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);
-        // dV += P^T dO and dK += dS^T Q, one half of the query columns per
-        // warpgroup as soon as that warpgroup has written it.
+        umma_commit(dp_full);
+        // dV += P^T dO, one half of the queries as soon as its warpgroup wrote P^T.
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull))) break;
@@ -307,7 +319,14 @@ __global__ void __launch_bounds__(320, 1)
             umma_ts(tmem + C::T_DV, tmem + C::T_ST + bwd_packed_col(kk),
                     smem_desc_sw128(do_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
                     (n > 0 || kk > 0) ? 1u : 0u);
-          if (g == 1) umma_commit(dv_done);
+        }
+        if (!ok) break;
+        umma_commit(dv_done);
+        // dK += dS^T Q, likewise per half.
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull))) break;
+          tc_fence_after_sync();
 #pragma unroll
           for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
             umma_ts(tmem + C::T_DK, tmem + C::T_DPT + bwd_packed_col(kk),
@@ -331,6 +350,7 @@ __global__ void __launch_bounds__(320, 1)
     const int r = wq * 32 + lane;  // key row in the tile
     const int kj = key0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tST = tmem + lane_off + C::T_ST + 64 * g, tDPT = tmem + lane_off + C::T_DPT + 64 * g;
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int n = 0; ok && n < n_steps; ++n) {
@@ -341,23 +361,23 @@ __global__ void __launch_bounds__(320, 1)
       // here too (already complete) so the copy's writes are visible.
       if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
       tc_fence_after_sync();
-      const float4* ldp = reinterpret_cast<const float4*>(sLD + s * C::LD_BYTES) + 32 * g;
+      const uint32_t ldp = smem_u32(sLD + s * C::LD_BYTES) + 512 * g;  // (lse2, Dl) x 2 columns per 16 bytes
       // query q0 + 64g + c sees key kj iff c >= kj - causal_offset - q0 - 64g
       const bool need_mask = a.causal && key0 + 127 > q0 + 64 * g + a.causal_offset;
       const int cmin = kj - a.causal_offset - q0 - 64 * g;
+      // ---- phase 1: P^T = exp2(S^T scale log2 e - lse2), kept in fp32 for phase 2
+      float p[64];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + C::T_ST + 64 * g + 32 * pass, sr);
-        tmem_ld32(tmem + lane_off + C::T_DPT + 64 * g + 32 * pass, dr);
+        uint32_t sr[32];
+        tmem_ld32(tST + 32 * pass, sr);
         tmem_wait_ld();
         tmem_reg_fence(sr);
-        tmem_reg_fence(dr);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
-          const float4 L = ldp[16 * pass + i];  // (lse2_c, Dl_c, lse2_c+1, Dl_c+1), same for the whole warp
+          const float4 L = lds_f4(ldp + 16 * (c >> 1));  // (lse2_c, Dl_c, lse2_c+1, Dl_c+1): a broadcast
           float x0, x1;
           fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -L.x, -L.z);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -365,18 +385,38 @@ __global__ void __launch_bounds__(320, 1)
             p0 = c < cmin ? 0.f : p0;
             p1 = c + 1 < cmin ? 0.f : p1;
           }
-          const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - L.y);
-          const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - L.w);
+          p[c] = p0;
+          p[c + 1] = p1;
           pk[i] = pack_bf16x2(p0, p1);
-          dk[i] = pack_bf16x2(ds0, ds1);
         }
-        // Packed over columns this warpgroup has already read.
-        tmem_st16(tmem + lane_off + C::T_ST + 64 * g + 16 * pass, pk);
-        tmem_st16(tmem + lane_off + C::T_DPT + 64 * g + 16 * pass, dk);
+        tmem_st16(tST + 16 * pass, pk);  // over columns this warpgroup has already read
       }
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(p_full + g);
+      // ---- phase 2: dS^T = P^T (dP^T - Dl)
+      if (!(ok = mbar_wait(dp_full, n & 1, a.status, kSiteBwdDpFull))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t dr[32];
+        tmem_ld32(tDPT + 32 * pass, dr);
+        tmem_wait_ld();
+        tmem_reg_fence(dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * pass + 2 * i;
+          const float4 L = lds_f4(ldp + 16 * (c >> 1));
+          float d0, d1;
+          fma2(d0, d1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), 1.f, 1.f, -L.y, -L.w);
+          dk[i] = pack_bf16x2(p[c] * d0, p[c + 1] * d1);
+        }
+        tmem_st16(tDPT + 16 * pass, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(ds_full + g);
     }
     if (!ok) *abort_flag = 1;
     // ---------------------------------------------------------- epilogue
@@ -420,9 +460,10 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_full = bars;
   uint64_t* full = bars + 1;
   uint64_t* empty = full + C::STAGES;
-  uint64_t* s_full = empty + C::STAGES;
-  uint64_t* p_full = s_full + 1;  // [2]
-  uint64_t* dq_done = p_full + 2;
+  uint64_t* s_full = empty + C::STAGES;  // [2], one per S buffer
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* ds_full = dp_full + 1;       // [2] warpgroup g wrote dS of its half
+  uint64_t* dq_done = ds_full + 2;
   uint64_t* acc_done = dq_done + 1;
   uint64_t* drain = acc_done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::Q_MISC_OFF);
@@ -448,8 +489,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(p_full + 1, 128);
+    mbar_init(s_full + 1, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(ds_full + 1, 128);
     mbar_init(dq_done, 1);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
@@ -501,7 +544,8 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-      auto issue_s = [&](int n) {  // S(n) = Q K_n^T into S buffer n & 1
+      // S(n) = Q K_n^T into S buffer n & 1; its barrier is s_full[n & 1].
+      auto issue_s = [&](int n) {
         const uint32_t k_addr = smem_u32(sK + (n % C::STAGES) * C::TILE_BYTES);
         const uint32_t dst = tmem + ((n & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
@@ -510,6 +554,7 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss(dst, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024), idesc_ss,
                   kk > 0 ? 1u : 0u);
         }
+        umma_commit(s_full + (n & 1));
       };
       bool ok = mbar_wait(q_full, 0, a.status, kSiteBwdQFull) && mbar_wait(full, 0, a.status, kSiteBwdFull);
       if (ok) {
@@ -518,7 +563,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int n = 0; ok && n < n_kt; ++n) {
         const int s = n % C::STAGES;
-        // dP overwrites dS of the previous step (read by its dQ MMAs).
+        // dP(n) overwrites dS(n-1) (read by dQ(n-1)).
         if (n > 0 && !(ok = mbar_wait(dq_done, (n - 1) & 1, a.status, kSiteBwdDqDone))) break;
         tc_fence_after_sync();
         const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
@@ -528,10 +573,9 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss(tmem + C::T_DP, smem_desc_sw128(do_addr + off, 16, 1024), smem_desc_sw128(v_addr + off, 16, 1024),
                   idesc_ss, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);  // S(n) and dP(n)
-        // S(n+1) into the other buffer (its previous contents, S(n-1), were
-        // read before the elementwise warps signalled step n-1) while the
-        // elementwise warps work on step n.
+        umma_commit(dp_full);
+        // S(n+1) into the other buffer, whose S(n-1) the elementwise warps read
+        // before signalling dS(n-1), which was waited for before dQ(n-1).
         if (n + 1 < n_kt) {
           if (!(ok = mbar_wait(full + (n + 1) % C::STAGES, ((n + 1) / C::STAGES) & 1, a.status, kSiteBwdFull)))
             break;
@@ -541,7 +585,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull))) break;
+          if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull))) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
@@ -565,6 +609,7 @@ __global__ void __launch_bounds__(320, 1)
     const int r = wq * 32 + lane;
     const int qi = q0 + r;  // < Nq_pad
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tDP = tmem + lane_off + C::T_DP + 64 * g;
     const float sl2 = a.scale_log2;
     const float2 L = a.ld[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
     const float lse2 = L.x, dl = L.y;
@@ -575,21 +620,20 @@ __global__ void __launch_bounds__(320, 1)
     const long long lim_first = a.causal ? min((long long)a.Nk - 1, (long long)q0 + a.causal_offset) : a.Nk - 1;
     bool ok = true;
     for (int n = 0; ok && n < n_kt; ++n) {
-      if (!(ok = mbar_wait(s_full, n & 1, a.status, kSiteBwdSFull))) break;
+      if (!(ok = mbar_wait(s_full + (n & 1), (n >> 1) & 1, a.status, kSiteBwdSFull))) break;
       tc_fence_after_sync();
       const uint32_t tS = tmem + lane_off + ((n & 1) ? C::T_S1 : C::T_S0) + 64 * g;
       const int kbase = n * 128 + 64 * g;
       const bool need_mask = kbase + 63 > lim_first;
       const int cmax = lim - kbase;  // column c is visible iff c <= cmax
+      // ---- phase 1: P = exp2(S scale log2 e - lse2)
+      float p[64];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32];
         tmem_ld32(tS + 32 * pass, sr);
-        tmem_ld32(tmem + lane_off + C::T_DP + 64 * g + 32 * pass, dr);
         tmem_wait_ld();
         tmem_reg_fence(sr);
-        tmem_reg_fence(dr);
-        uint32_t dk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
@@ -600,13 +644,32 @@ __global__ void __launch_bounds__(320, 1)
             p0 = c > cmax ? 0.f : p0;
             p1 = c + 1 > cmax ? 0.f : p1;
           }
-          dk[i] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * i]) - dl), p1 * (__uint_as_float(dr[2 * i + 1]) - dl));
+          p[c] = p0;
+          p[c + 1] = p1;
         }
-        tmem_st16(tmem + lane_off + C::T_DP + 64 * g + 16 * pass, dk);
+      }
+      // ---- phase 2: dS = P (dP - Dl), packed over this half's first 32 columns of dP
+      if (!(ok = mbar_wait(dp_full, n & 1, a.status, kSiteBwdDpFull))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t dr[32];
+        tmem_ld32(tDP + 32 * pass, dr);
+        tmem_wait_ld();
+        tmem_reg_fence(dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * pass + 2 * i;
+          float d0, d1;
+          fma2(d0, d1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), 1.f, 1.f, -dl, -dl);
+          dk[i] = pack_bf16x2(p[c] * d0, p[c + 1] * d1);
+        }
+        tmem_st16(tDP + 16 * pass, dk);
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(p_full + g);
+      mbar_arrive(ds_full + g);
     }
     if (!ok) *abort_flag = 1;
     // ---------------------------------------------------------- epilogue
