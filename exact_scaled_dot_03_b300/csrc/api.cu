@@ -252,18 +252,18 @@ attn_status dispatch_decode_gc(const void* q, const void* kc, const void* vc, co
 }  // namespace
 
 namespace {
-// Backward workspace: (lse2, Dl) per query row, each head padded to 128 rows.
+// Backward workspace: lse2 then Dl (fp32) per query row, each head padded to 128 rows.
 bool plan_bwd(int B, int Hq, int Nq, int* Nq_pad, size_t* bytes) {
   if (B < 1 || Hq < 1 || Nq < 0) return false;
   *Nq_pad = (Nq + 127) / 128 * 128;
-  *bytes = static_cast<size_t>(B) * Hq * static_cast<size_t>(*Nq_pad) * sizeof(float2);
+  *bytes = static_cast<size_t>(B) * Hq * static_cast<size_t>(*Nq_pad) * 2 * sizeof(float);
   return true;
 }
 
 template <int D>
 attn_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-                       float2* ld, int Nq_pad, cudaStream_t s, int dev) {
+                       float* ws, int Nq_pad, cudaStream_t s, int dev) {
   using C = BwdCfg<D>;
   static bool smem_kv[kMaxDevices] = {}, smem_q[kMaxDevices] = {};
   CUtensorMap tq, tk, tv, tdo;
@@ -279,7 +279,9 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
-  a.ld = ld;
+  const long long rows = static_cast<long long>(B) * Hq * Nq_pad;
+  a.lse2 = ws;
+  a.dl = ws + rows;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -298,7 +300,8 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   const long long threads = heads * Nq_pad * (D / 8);
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
   bwd_prep_kernel<D><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                            static_cast<const __nv_bfloat16*>(dout), lse, ld, heads, Nq, Nq_pad);
+                                            static_cast<const __nv_bfloat16*>(dout), lse, ws, ws + rows, heads, Nq,
+                                            Nq_pad);
   attn_bwd_dkdv_kernel<D><<<dim3(Hkv, (Nk + 127) / 128, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -451,10 +454,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     }
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  float2* ld = static_cast<float2*>(workspace);
+  float* ws = static_cast<float*>(workspace);
   if (d == 64)
-    return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ld, Nq_pad, s, dev);
-  return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ld, Nq_pad, s, dev);
+    return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ws, Nq_pad, s, dev);
+  return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, scale, causal, ws, Nq_pad, s, dev);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d) {

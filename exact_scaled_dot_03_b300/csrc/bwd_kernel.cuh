@@ -13,9 +13,9 @@
 // [MG-B] menggq.pages.dev "Transformer 深度进阶：从矩阵视角到 FlashAttention 工程优化".
 //
 // Three kernels, no atomics (the result is deterministic):
-//   bwd_prep_kernel      per query row: (lse * log2 e, Dl), each head padded to
-//                        a multiple of 128 rows with (+inf, 0) so that padded
-//                        rows get P = 0.
+//   bwd_prep_kernel      per query row: lse * log2 e and Dl (two arrays), each
+//                        head padded to a multiple of 128 rows with +inf and 0
+//                        so that padded rows get P = 0.
 //   attn_bwd_dkdv_kernel CTA = one 128-key tile of one (batch, KV head). It
 //                        streams every query tile of every query head of the
 //                        group; dK and dV accumulate in TMEM.
@@ -43,7 +43,8 @@ struct BwdArgs {
   __nv_bfloat16* dq;   // [B, Hq, Nq, D]
   __nv_bfloat16* dk;   // [B, Hkv, Nk, D]
   __nv_bfloat16* dv;   // [B, Hkv, Nk, D]
-  const float2* ld;    // [B * Hq][Nq_pad]: (lse * log2 e, Dl); padded rows (+inf, 0)
+  const float* lse2;   // [B * Hq][Nq_pad]: lse * log2 e; padded rows +inf
+  const float* dl;     // [B * Hq][Nq_pad]: Dl = sum_t dO_t O_t; padded rows 0
   int B, Hq, Hkv, Nq, Nk, Nq_pad;
   int group;           // Hq / Hkv
   int causal;
@@ -60,7 +61,7 @@ struct BwdCfg {
   static constexpr int BLOCK_BYTES = 128 * 64 * 2;   // 128 rows x 64 columns, 128-byte swizzle
   static constexpr int TILE_BYTES = KBLK * BLOCK_BYTES;
   static constexpr int STAGES = (D == 128) ? 2 : 4;
-  static constexpr int LD_BYTES = 128 * 8;           // (lse2, Dl) of 128 query rows
+  static constexpr int LD_BYTES = 128 * 8;           // lse2[128] then Dl[128] of a query tile
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
 
@@ -111,8 +112,8 @@ __device__ __forceinline__ uint32_t bwd_packed_col(int kk) { return (kk >> 2) * 
 // One 16-byte chunk per thread; the D/8 threads of a row reduce by shuffles.
 template <int D>
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                const float* __restrict__ lse, float2* __restrict__ ld, long long heads, int Nq,
-                                int Nq_pad) {
+                                const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dl,
+                                long long heads, int Nq, int Nq_pad) {
   constexpr int TPR = D / 8;
   const long long n = heads * Nq_pad * TPR;
   const long long stride = (long long)gridDim.x * blockDim.x;  // a multiple of 32
@@ -139,13 +140,13 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_
 #pragma unroll
     for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (valid && c == 0) {
-      float2 r = make_float2(CUDART_INF_F, 0.f);
+      float l2 = CUDART_INF_F;
       if (i < Nq) {
         const float l = lse[(size_t)hh * Nq + i];
-        r.x = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
-        r.y = acc;
+        l2 = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
       }
-      ld[(size_t)hh * Nq_pad + i] = r;
+      lse2[(size_t)hh * Nq_pad + i] = l2;
+      dl[(size_t)hh * Nq_pad + i] = i < Nq ? acc : 0.f;
     }
   }
 }
@@ -266,7 +267,9 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(sQ + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, full + s, kb * 64, q0, b * a.Hq + h);
           tma_load_3d(sDO + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_do, full + s, kb * 64, q0, b * a.Hq + h);
         }
-        bulk_load(sLD + s * C::LD_BYTES, a.ld + (size_t)(b * a.Hq + h) * a.Nq_pad + q0, C::LD_BYTES, full + s);
+        const size_t row0 = (size_t)(b * a.Hq + h) * a.Nq_pad + q0;
+        bulk_load(sLD + s * C::LD_BYTES, a.lse2 + row0, C::LD_BYTES / 2, full + s);
+        bulk_load(sLD + s * C::LD_BYTES + C::LD_BYTES / 2, a.dl + row0, C::LD_BYTES / 2, full + s);
         issued = n + 1;
         if (*abort_flag) break;
       }
@@ -361,7 +364,8 @@ __global__ void __launch_bounds__(320, 1)
       // here too (already complete) so the copy's writes are visible.
       if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
       tc_fence_after_sync();
-      const uint32_t ldp = smem_u32(sLD + s * C::LD_BYTES) + 512 * g;  // (lse2, Dl) x 2 columns per 16 bytes
+      // lse2 and Dl of this half's 64 query columns, four per 16-byte load (broadcasts)
+      const uint32_t lsp = smem_u32(sLD + s * C::LD_BYTES) + 256 * g, dlp = lsp + C::LD_BYTES / 2;
       // query q0 + 64g + c sees key kj iff c >= kj - causal_offset - q0 - 64g
       const bool need_mask = a.causal && key0 + 127 > q0 + 64 * g + a.causal_offset;
       const int cmin = kj - a.causal_offset - q0 - 64 * g;
@@ -374,12 +378,14 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         tmem_reg_fence(sr);
         uint32_t pk[16];
+        float4 L;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
-          const float4 L = lds_f4(ldp + 16 * (c >> 1));  // (lse2_c, Dl_c, lse2_c+1, Dl_c+1): a broadcast
+          if ((i & 1) == 0) L = lds_f4(lsp + 4 * c);  // lse2 of columns c .. c+3
+          const float l0 = (i & 1) ? L.z : L.x, l1 = (i & 1) ? L.w : L.y;
           float x0, x1;
-          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -L.x, -L.z);
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -l0, -l1);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (need_mask) {
             p0 = c < cmin ? 0.f : p0;
@@ -404,12 +410,14 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         tmem_reg_fence(dr);
         uint32_t dk[16];
+        float4 L;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
-          const float4 L = lds_f4(ldp + 16 * (c >> 1));
+          if ((i & 1) == 0) L = lds_f4(dlp + 4 * c);  // Dl of columns c .. c+3
+          const float e0 = (i & 1) ? L.z : L.x, e1 = (i & 1) ? L.w : L.y;
           float d0, d1;
-          fma2(d0, d1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), 1.f, 1.f, -L.y, -L.w);
+          fma2(d0, d1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), 1.f, 1.f, -e0, -e1);
           dk[i] = pack_bf16x2(p[c] * d0, p[c + 1] * d1);
         }
         tmem_st16(tDPT + 16 * pass, dk);
@@ -611,8 +619,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tDP = tmem + lane_off + C::T_DP + 64 * g;
     const float sl2 = a.scale_log2;
-    const float2 L = a.ld[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
-    const float lse2 = L.x, dl = L.y;
+    const float lse2 = a.lse2[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
+    const float dl = a.dl[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
     // last key this row sees (keys past it are masked)
     const long long lim_ll = a.causal ? min((long long)a.Nk - 1, (long long)qi + a.causal_offset) : a.Nk - 1;
     const int lim = (int)max(lim_ll, -1LL);
