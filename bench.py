@@ -1,14 +1,16 @@
 """Benchmark: exact causal attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--prefill NAME] [--only prefill|decode] [--no-cpu-baseline] [--no-e2e]
+                    [--prefill NAME] [--only prefill|decode|paged|window|backward]
+                    [--no-cpu-baseline] [--no-e2e]
 
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
 already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
 N=16384, d=128), a decode step (B=16, Hq=32, Hkv=8, d=128, cache lengths
 uniform on [1024, 8192]), the same decode over a paged cache (64-token
-pages) with the new token appended, and the prefill again with a 4096-key
-causal sliding window. L2 is flushed (a 256 MiB write) before each
+pages) with the new token appended, the prefill again with a 4096-key
+causal sliding window, and the backward pass of the causal prefill (dQ, dK,
+dV from the o and lse that step's prefill wrote and a seeded dO). L2 is flushed (a 256 MiB write) before each
 of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
 read so the timed kernel does not pay for writing back the flush's dirty lines.
 Prints one JSON line.
@@ -251,14 +253,17 @@ def run_ours(args, w, wd):
     do_dec = args.only in (None, "decode")
     do_pag = args.only in (None, "paged")
     do_win = args.only in (None, "window")
+    do_bwd = args.only in (None, "backward")
 
     parts = []  # (name, launch function)
-    if do_pre:
+    kernels = {"prefill": 1, "decode": 1, "window": 1, "paged": 1, "backward": 3}  # our launches per call
+    if do_pre or do_bwd:
         q_h, k_h, v_h = W.prefill_inputs(w)
         q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
         o = torch.empty_like(q)
         lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
-        parts.append(("prefill", lambda: binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)))
+        if do_pre:
+            parts.append(("prefill", lambda: binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)))
     if do_dec:
         dq_h, kc_h, vc_h, sl_h = W.decode_inputs(wd)
         dq, kc, vc, sl = dq_h.to(dev), kc_h.to(dev), vc_h.to(dev), sl_h.to(dev)
@@ -289,6 +294,19 @@ def run_ours(args, w, wd):
         # lengths are not advanced between timed calls, so the work is identical).
         parts.append(("paged", lambda: binding.decode_paged(pq, pkp, pvp, pbt, psl, pkn, pvn, scale=wp.scale,
                                                             workspace=pws, out=po, lse=plse)))
+    if do_bwd:
+        dout = W.backward_inputs(w)[3].to(dev)   # Q, K, V are the prefill's draw; dO follows them
+        binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)  # o, lse (rewritten each step)
+        bws = torch.empty(max(1, int(binding.lib().attn_bwd_workspace_size(w.B, w.Hq, w.Nq))), dtype=torch.uint8,
+                          device=dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        parts.append(("backward", lambda: binding.bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale,
+                                                      workspace=bws, dq=gq, dk=gk, dv=gv)))
+    # The backward is timed in its own loop after the others: its seconds of
+    # full tensor load would otherwise hold the part at its power cap while
+    # the prefill is timed.
+    groups = [[p for p in parts if p[0] != "backward"], [p for p in parts if p[0] == "backward"]]
+    groups = [g for g in groups if g]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     clean_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -308,31 +326,40 @@ def run_ours(args, w, wd):
     if code != binding.OK:
         raise RuntimeError(f"device status after warm-up: {code} {detail}")
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
-          for _ in range(args.steps)]
     sampler = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
-    # Keep the device busy while the host queues the timed launches, so no
-    # event bracket contains host launch latency (that is the e2e number's job).
-    torch.cuda._sleep(int(2e9 * (0.01 + 0.0004 * args.steps * len(parts))))
-    t_wall = time.perf_counter()
-    for step in ev:
-        for (e0, e1), (_, fn) in zip(step, parts):
-            flush_l2()           # outside the event bracket
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
+    ms = {}
+    t_wall = 0.0
+    for gi, group in enumerate(groups):
+        if gi > 0:  # the later group gets its own warm-up
+            for _ in range(args.warmup):
+                for _, fn in group:
+                    flush_l2()
+                    fn()
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in group]
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        # Keep the device busy while the host queues the timed launches, so no
+        # event bracket contains host launch latency (that is the e2e number's job).
+        torch.cuda._sleep(int(2e9 * (0.01 + 0.0004 * args.steps * len(group))))
+        t0 = time.perf_counter()
+        for step in ev:
+            for (e0, e1), (_, fn) in zip(step, group):
+                flush_l2()           # outside the event bracket
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall += time.perf_counter() - t0
+        ms.update({name: [step[i][0].elapsed_time(step[i][1]) for step in ev] for i, (name, _) in enumerate(group)})
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = {name: [step[i][0].elapsed_time(step[i][1]) for step in ev] for i, (name, _) in enumerate(parts)}
-    launches = len(parts) * args.steps
+    launches = sum(kernels[name] for name, _ in parts) * args.steps
     code, detail = binding.device_status()
     if code != binding.OK:
         raise RuntimeError(f"device status after the timed steps: {code} {detail}")
@@ -404,6 +431,25 @@ def run_ours(args, w, wd):
         if not do_pre and not do_dec:
             value, unit, roofline = pag_value, "GB/s", pag_roof
 
+    bwd_block = None
+    if do_bwd:
+        # The usual convention for the backward: 2.5x the forward's FLOPs (five
+        # products of the forward's size: S, dP, dV, dK, dQ); the recomputation
+        # of S and dP in the dQ kernel is not counted.
+        bwd_flops = 2.5 * w.flops()
+        bwd_value = world * bwd_flops * args.steps / (tot["backward"] / 1e3) / 1e12
+        bwd_achieved = bwd_flops / (statistics.mean(ms["backward"]) / 1e3) / 1e12
+        bwd_roof = {"bound": "tensor", "achieved": bwd_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": bwd_achieved / peaks["bf16_tflops"],
+                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)", "traffic": None,
+                    "algorithmic_flops_per_launch": bwd_flops,
+                    "kernel": "bwd_prep_kernel<128> + attn_bwd_dkdv_kernel<128> + attn_bwd_dq_kernel<128>"}
+        bwd_block = {"metric": "causal attention backward TFLOP/s (2.5x forward FLOPs)", "workload": w.name,
+                     "value": bwd_value, "unit": "TFLOP/s", "ms": tot["backward"] / args.steps,
+                     "roofline": bwd_roof}
+        if not (do_pre or do_dec or do_pag or do_win):
+            value, unit, roofline = bwd_value, "TFLOP/s", bwd_roof
+
     e2e = None
     if do_pre and not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
         e2e = measure_e2e(args, w, q_h, k_h, v_h, dev)
@@ -420,7 +466,8 @@ def run_ours(args, w, wd):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16)",
             "config": {"workload": (w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name if do_pag
-                                    else f"{W.CAUSAL_GQA_16384.name}_window{WINDOW}"),
+                                    else f"{W.CAUSAL_GQA_16384.name}_window{WINDOW}" if do_win
+                                    else f"{w.name}_backward"),
                        "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         }
@@ -435,6 +482,8 @@ def run_ours(args, w, wd):
             line["decode_paged"] = pag_block
         if win_block is not None and (do_pre or do_dec or do_pag):
             line["prefill_window"] = win_block
+        if bwd_block is not None and (do_pre or do_dec or do_pag or do_win):
+            line["backward"] = bwd_block
         line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
                      "clocks": clocks, "wall_s_timed_region": t_wall})
         print(json.dumps(line), flush=True)
@@ -487,7 +536,7 @@ def main():
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window", "backward"], default=None,
                     help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
