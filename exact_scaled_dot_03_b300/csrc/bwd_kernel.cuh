@@ -434,6 +434,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after_sync();
       if (*abort_flag) have = false;
     }
+    have = __all_sync(0xffffffffu, have);  // guards warp-collective TMEM loads
     // warpgroup 0 writes dV, warpgroup 1 writes dK (times the score scale)
     const bool in_range = kj < a.Nk;
     __nv_bfloat16* dst = (g == 0 ? a.dv : a.dk) + ((size_t)(b * a.Hkv + hkv) * a.Nk + (in_range ? kj : 0)) * D;
@@ -687,6 +688,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after_sync();
       if (*abort_flag) have = false;
     }
+    have = __all_sync(0xffffffffu, have);  // guards warp-collective TMEM loads
     const bool in_range = qi < a.Nq;
     __nv_bfloat16* dst = a.dq + ((size_t)(b * a.Hq + h) * a.Nq + (in_range ? qi : 0)) * D;
     // warpgroup g writes columns [g D/2, (g+1) D/2)

@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after_sync();
       have_o = ok;
     }
+    have_o = __all_sync(0xffffffffu, have_o);  // guards warp-collective TMEM loads
     const bool in_range = row < a.Nq;
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = a.o + ((size_t)(b * a.Hq + h) * a.Nq + (in_range ? row : 0)) * D;
