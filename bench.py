@@ -441,7 +441,9 @@ def run_ours(args, w, wd):
         bwd_achieved = bwd_flops / (statistics.mean(ms["backward"]) / 1e3) / 1e12
         bwd_roof = {"bound": "tensor", "achieved": bwd_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": bwd_achieved / peaks["bf16_tflops"],
-                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)", "traffic": None,
+                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                    "traffic": profiled_traffic("attn_bwd_causal_gqa_traffic.txt", ("bwd_kernel.cuh", "ptx.cuh")),
+                    "traffic_note": "DRAM bytes of one backward call (dK/dV + dQ kernels), from the ncu capture",
                     "algorithmic_flops_per_launch": bwd_flops,
                     "kernel": "bwd_prep_kernel<128> + attn_bwd_dkdv_kernel<128> + attn_bwd_dq_kernel<128>"}
         bwd_block = {"metric": "causal attention backward TFLOP/s (2.5x forward FLOPs)", "workload": w.name,
