@@ -252,9 +252,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      const uint64_t stream_once = l2_policy_evict_first();  // this key tile is read by this CTA only
       for (int kb = 0; kb < C::KBLK; ++kb) {
-        tma_load_3d(sK + kb * C::BLOCK_BYTES, &tm_k, kv_full, kb * 64, key0, b * a.Hkv + hkv);
-        tma_load_3d(sV + kb * C::BLOCK_BYTES, &tm_v, kv_full, kb * 64, key0, b * a.Hkv + hkv);
+        tma_load_3d_hint(sK + kb * C::BLOCK_BYTES, &tm_k, kv_full, kb * 64, key0, b * a.Hkv + hkv, stream_once);
+        tma_load_3d_hint(sV + kb * C::BLOCK_BYTES, &tm_v, kv_full, kb * 64, key0, b * a.Hkv + hkv, stream_once);
       }
       int issued = 0;
       for (int n = 0; n < n_steps; ++n) {
@@ -523,9 +524,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+      const uint64_t stream_once = l2_policy_evict_first();  // this query tile is read by this CTA only
       for (int kb = 0; kb < C::KBLK; ++kb) {
-        tma_load_3d(sQ + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q0, b * a.Hq + h);
-        tma_load_3d(sDO + kb * C::BLOCK_BYTES, &tm_do, q_full, kb * 64, q0, b * a.Hq + h);
+        tma_load_3d_hint(sQ + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q0, b * a.Hq + h, stream_once);
+        tma_load_3d_hint(sDO + kb * C::BLOCK_BYTES, &tm_do, q_full, kb * 64, q0, b * a.Hq + h, stream_once);
       }
       int issued = 0;
       for (int n = 0; n < n_kt; ++n) {

@@ -192,11 +192,12 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qbytes = 0;
       for (int t = 0; t < 2; ++t) qbytes += n_kv[t] > 0 ? C::TILE_BYTES : 0;
       mbar_arrive_expect_tx(q_full, qbytes);
+      const uint64_t stream_once = l2_policy_evict_first();  // Q is read by this CTA only
       for (int t = 0; t < 2; ++t) {
         if (n_kv[t] == 0) continue;
         for (int kb = 0; kb < C::KBLK; ++kb)
-          tma_load_3d(sQ + t * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q_base + 128 * t,
-                      b * a.Hq + h);
+          tma_load_3d_hint(sQ + t * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q_base + 128 * t,
+                           b * a.Hq + h, stream_once);
       }
       int issued = 0;
       for (int js = 0; js < n_kv_max; ++js) {
