@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(320, 1)
     have_o = __all_sync(0xffffffffu, have_o);  // guards warp-collective TMEM loads
     const bool in_range = row < a.Nq;
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const uint64_t out_policy = l2_policy_evict_first();
     __nv_bfloat16* orow = a.o + ((size_t)(b * a.Hq + h) * a.Nq + (in_range ? row : 0)) * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -452,8 +453,9 @@ __global__ void __launch_bounds__(320, 1)
       if (in_range) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)  // O is written once: evict-first keeps K/V of other CTAs in L2
+          st_global_v4_hint(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]),
+                            out_policy);
       }
     }
     if (a.lse != nullptr && in_range) {
