@@ -1,7 +1,7 @@
 """Benchmark: exact causal attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--prefill NAME] [--only prefill|decode|paged|window|backward]
+                    [--prefill NAME] [--only prefill|decode|paged|window|backward|rope]
                     [--no-cpu-baseline] [--no-e2e]
 
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
@@ -10,7 +10,8 @@ N=16384, d=128), a decode step (B=16, Hq=32, Hkv=8, d=128, cache lengths
 uniform on [1024, 8192]), the same decode over a paged cache (64-token
 pages) with the new token appended, the prefill again with a 4096-key
 causal sliding window, and the backward pass of the causal prefill (dQ, dK,
-dV from the o and lse that step's prefill wrote and a seeded dO). L2 is flushed (a 256 MiB write) before each
+dV from the o and lse that step's prefill wrote and a seeded dO) and the prefill
+with rotary position embedding (base 10000) in a second loop. L2 is flushed (a 256 MiB write) before each
 of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
 read so the timed kernel does not pay for writing back the flush's dirty lines.
 Prints one JSON line.
@@ -254,10 +255,11 @@ def run_ours(args, w, wd):
     do_pag = args.only in (None, "paged")
     do_win = args.only in (None, "window")
     do_bwd = args.only in (None, "backward")
+    do_rope = args.only in (None, "rope")
 
     parts = []  # (name, launch function)
-    kernels = {"prefill": 1, "decode": 1, "window": 1, "paged": 1, "backward": 3}  # our launches per call
-    if do_pre or do_bwd:
+    kernels = {"prefill": 1, "decode": 1, "window": 1, "paged": 1, "backward": 3, "rope": 3}  # our launches per call
+    if do_pre or do_bwd or do_rope:
         q_h, k_h, v_h = W.prefill_inputs(w)
         q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
         o = torch.empty_like(q)
@@ -302,10 +304,18 @@ def run_ours(args, w, wd):
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         parts.append(("backward", lambda: binding.bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale,
                                                       workspace=bws, dq=gq, dk=gk, dv=gv)))
-    # The backward is timed in its own loop after the others: its seconds of
-    # full tensor load would otherwise hold the part at its power cap while
-    # the prefill is timed.
-    groups = [[p for p in parts if p[0] != "backward"], [p for p in parts if p[0] == "backward"]]
+    if do_rope:
+        rws = torch.empty(int(binding.lib().attn_fwd_rope_workspace_size(w.B, w.Hkv, w.Nq, w.Nk, w.d)),
+                          dtype=torch.uint8, device=dev)
+        ro = torch.empty_like(q)
+        rlse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+        parts.append(("rope", lambda: binding.fwd_rope(q, k, v, causal=w.causal, scale=w.scale, base=10000.0,
+                                                       workspace=rws, out=ro, lse=rlse)))
+    # The backward and RoPE prefill are timed in their own loop after the
+    # others: their seconds of full tensor load would otherwise hold the part
+    # at its power cap while the prefill is timed.
+    later = ("backward", "rope")
+    groups = [[p for p in parts if p[0] not in later], [p for p in parts if p[0] in later]]
     groups = [g for g in groups if g]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -452,6 +462,23 @@ def run_ours(args, w, wd):
         if not (do_pre or do_dec or do_pag or do_win):
             value, unit, roofline = bwd_value, "TFLOP/s", bwd_roof
 
+    rope_block = None
+    if do_rope:
+        # The pre-pass (table + rotated K) is inside the timed call; FLOPs are the prefill's.
+        rflops = w.flops()
+        rope_value = world * rflops * args.steps / (tot["rope"] / 1e3) / 1e12
+        rope_achieved = rflops / (statistics.mean(ms["rope"]) / 1e3) / 1e12
+        rope_roof = {"bound": "tensor", "achieved": rope_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": rope_achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)", "traffic": None,
+                     "algorithmic_flops_per_launch": rflops,
+                     "kernel": "rope_table_kernel<128> + rope_k_kernel<128> + attn_fwd_kernel<128> (RoPE on Q)"}
+        rope_block = {"metric": "causal prefill with RoPE TFLOP/s (prefill FLOPs; table and K rotation included)",
+                      "workload": f"{w.name}_rope10000", "value": rope_value, "unit": "TFLOP/s",
+                      "ms": tot["rope"] / args.steps, "roofline": rope_roof}
+        if args.only == "rope":
+            value, unit, roofline = rope_value, "TFLOP/s", rope_roof
+
     e2e = None
     if do_pre and not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
         e2e = measure_e2e(args, w, q_h, k_h, v_h, dev)
@@ -469,7 +496,7 @@ def run_ours(args, w, wd):
             "data": "synthetic (seeded N(0,1) bf16)",
             "config": {"workload": (w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name if do_pag
                                     else f"{W.CAUSAL_GQA_16384.name}_window{WINDOW}" if do_win
-                                    else f"{w.name}_backward"),
+                                    else f"{w.name}_backward" if do_bwd else f"{w.name}_rope10000"),
                        "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         }
@@ -486,6 +513,8 @@ def run_ours(args, w, wd):
             line["prefill_window"] = win_block
         if bwd_block is not None and (do_pre or do_dec or do_pag or do_win):
             line["backward"] = bwd_block
+        if rope_block is not None and args.only != "rope":
+            line["prefill_rope"] = rope_block
         line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
                      "clocks": clocks, "wall_s_timed_region": t_wall})
         print(json.dumps(line), flush=True)
@@ -538,7 +567,7 @@ def main():
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window", "backward"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window", "backward", "rope"], default=None,
                     help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
