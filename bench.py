@@ -240,6 +240,25 @@ def run_reference(args, w, wd):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- replicas
+def max_over_ranks(totals: dict, device) -> dict:
+    """Per-part timed totals (ms), element-wise max over all ranks: the job
+    is as fast as its slowest replica. Identity on a single process."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return dict(totals)
+    names = sorted(totals)
+    t = torch.tensor([totals[n] for n in names], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(names, t.tolist()))
+
+
+def job_rate(work_per_step: float, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job throughput: the work every replica did (each rank runs the
+    same workload: weak scaling) over the slowest rank's timed total."""
+    return world * work_per_step * steps / (total_ms / 1e3)
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_ours(args, w, wd):
     from exact_scaled_dot_03_b300 import binding
@@ -374,18 +393,14 @@ def run_ours(args, w, wd):
     if code != binding.OK:
         raise RuntimeError(f"device status after the timed steps: {code} {detail}")
 
-    tot = {name: sum(v) for name, v in ms.items()}
-    if world > 1:
-        t = torch.tensor([tot[n] for n, _ in parts], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot = {n: x for (n, _), x in zip(parts, t.tolist())}
+    tot = max_over_ranks({name: sum(v) for name, v in ms.items()}, dev)
     peaks = measured_peaks()
 
     roofline = dec_block = None
     value = unit = None
     if do_pre:
         flops = w.flops()
-        value = world * flops * args.steps / (tot["prefill"] / 1e3) / 1e12
+        value = job_rate(flops, args.steps, world, tot["prefill"]) / 1e12
         unit = "TFLOP/s"
         achieved = flops / (statistics.mean(ms["prefill"]) / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -398,7 +413,7 @@ def run_ours(args, w, wd):
                     "algorithmic_flops_per_launch": flops, "kernel": "attn_fwd_kernel<128>"}
     if do_dec:
         dec_bytes = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
-        dec_value = world * dec_bytes * args.steps / (tot["decode"] / 1e3) / 1e9
+        dec_value = job_rate(dec_bytes, args.steps, world, tot["decode"]) / 1e9
         dec_achieved = dec_bytes / (statistics.mean(ms["decode"]) / 1e3) / 1e9
         dec_roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": dec_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
@@ -414,7 +429,7 @@ def run_ours(args, w, wd):
         # FLOPs of the pairs that are actually visible: row i sees min(i+1, WINDOW) keys
         pairs = sum(min(i + 1, WINDOW) for i in range(ww.Nq))
         win_flops = 4.0 * ww.B * ww.Hq * ww.d * pairs
-        win_value = world * win_flops * args.steps / (tot["window"] / 1e3) / 1e12
+        win_value = job_rate(win_flops, args.steps, world, tot["window"]) / 1e12
         win_achieved = win_flops / (statistics.mean(ms["window"]) / 1e3) / 1e12
         win_roof = {"bound": "tensor", "achieved": win_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": win_achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
@@ -429,7 +444,7 @@ def run_ours(args, w, wd):
     if do_pag:
         pag_bytes = ((int(psl_h.sum()) + wp.B) * wp.Hkv * wp.d * 2 * 2 + 2 * wp.B * wp.Hq * wp.d * 2
                      + 4 * wp.B * wp.Hq + 2 * wp.B * wp.Hkv * wp.d * 2 * 2)
-        pag_value = world * pag_bytes * args.steps / (tot["paged"] / 1e3) / 1e9
+        pag_value = job_rate(pag_bytes, args.steps, world, tot["paged"]) / 1e9
         pag_achieved = pag_bytes / (statistics.mean(ms["paged"]) / 1e3) / 1e9
         pag_roof = {"bound": "hbm", "achieved": pag_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": pag_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
@@ -447,7 +462,7 @@ def run_ours(args, w, wd):
         # products of the forward's size: S, dP, dV, dK, dQ); the recomputation
         # of S and dP in the dQ kernel is not counted.
         bwd_flops = 2.5 * w.flops()
-        bwd_value = world * bwd_flops * args.steps / (tot["backward"] / 1e3) / 1e12
+        bwd_value = job_rate(bwd_flops, args.steps, world, tot["backward"]) / 1e12
         bwd_achieved = bwd_flops / (statistics.mean(ms["backward"]) / 1e3) / 1e12
         bwd_roof = {"bound": "tensor", "achieved": bwd_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": bwd_achieved / peaks["bf16_tflops"],
@@ -466,7 +481,7 @@ def run_ours(args, w, wd):
     if do_rope:
         # The pre-pass (table + rotated K) is inside the timed call; FLOPs are the prefill's.
         rflops = w.flops()
-        rope_value = world * rflops * args.steps / (tot["rope"] / 1e3) / 1e12
+        rope_value = job_rate(rflops, args.steps, world, tot["rope"]) / 1e12
         rope_achieved = rflops / (statistics.mean(ms["rope"]) / 1e3) / 1e12
         rope_roof = {"bound": "tensor", "achieved": rope_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": rope_achieved / peaks["bf16_tflops"],
