@@ -252,11 +252,13 @@ attn_status dispatch_decode_gc(const void* q, const void* kc, const void* vc, co
 }  // namespace
 
 namespace {
-// Backward workspace: lse2 then Dl (fp32) per query row, each head padded to 128 rows.
+// Backward workspace, per query row (each head padded to 128 rows): lse2 and Dl
+// (fp32, two arrays), then the dK/dV kernel's seed operands (32 bytes per row
+// and array, 4 KiB per 128-row tile).
 bool plan_bwd(int B, int Hq, int Nq, int* Nq_pad, size_t* bytes) {
   if (B < 1 || Hq < 1 || Nq < 0) return false;
   *Nq_pad = (Nq + 127) / 128 * 128;
-  *bytes = static_cast<size_t>(B) * Hq * static_cast<size_t>(*Nq_pad) * 2 * sizeof(float);
+  *bytes = static_cast<size_t>(B) * Hq * static_cast<size_t>(*Nq_pad) * (2 * sizeof(float) + 2 * 32);
   return true;
 }
 
@@ -282,6 +284,10 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   const long long rows = static_cast<long long>(B) * Hq * Nq_pad;
   a.lse2 = ws;
   a.dl = ws + rows;
+  uint8_t* seed_l = reinterpret_cast<uint8_t*>(ws + 2 * rows);
+  uint8_t* seed_d = seed_l + rows * 32;
+  a.seed_l = seed_l;
+  a.seed_d = seed_d;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -300,8 +306,8 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   const long long threads = heads * Nq_pad * (D / 8);
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
   bwd_prep_kernel<D><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                            static_cast<const __nv_bfloat16*>(dout), lse, ws, ws + rows, heads, Nq,
-                                            Nq_pad);
+                                            static_cast<const __nv_bfloat16*>(dout), lse, ws, ws + rows, seed_l,
+                                            seed_d, scale, heads, Nq, Nq_pad);
   attn_bwd_dkdv_kernel<D><<<dim3(Hkv, (Nk + 127) / 128, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

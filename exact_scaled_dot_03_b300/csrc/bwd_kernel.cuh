@@ -26,7 +26,10 @@
 // producer, warp 9 TMEM allocator + tcgen05.mma issuer. The elementwise work
 // of a step runs in two phases, P = exp2(S - lse) (the exponentials) as soon
 // as S is in TMEM and dS = P (dP - Dl) once dP is, so each phase overlaps a
-// different MMA group (all MMAs are M = N = 128):
+// different MMA group (all MMAs are M = N = 128). In the dK/dV kernel, where
+// lse and Dl belong to the columns, one extra K=16 MMA (a tile of ones times
+// the column values split into three bf16 parts) seeds S^T with -lse/scale and
+// dP^T with -Dl, so the elementwise warps load no per-column value:
 //   dK/dV step: S^T | dP^T (P phase) | dV (dS phase) | dK
 //   dQ step:    dP(n) (P phase) | S(n+1) (dS phase) | dQ(n)
 // (S double-buffered in the dQ kernel so the next one is already queued).
@@ -45,6 +48,11 @@ struct BwdArgs {
   __nv_bfloat16* dv;   // [B, Hkv, Nk, D]
   const float* lse2;   // [B * Hq][Nq_pad]: lse * log2 e; padded rows +inf
   const float* dl;     // [B * Hq][Nq_pad]: Dl = sum_t dO_t O_t; padded rows 0
+  // Per 128-row query tile, the K=16 B operands that seed the dK/dV kernel's
+  // accumulators (layout: bwd_seed_offset): -lse/scale and -Dl, each split
+  // into three bf16 parts (columns 0-2; 3-15 zero). 4 KiB per tile and array.
+  const uint8_t* seed_l;
+  const uint8_t* seed_d;
   int B, Hq, Hkv, Nq, Nk, Nq_pad;
   int group;           // Hq / Hkv
   int causal;
@@ -61,7 +69,7 @@ struct BwdCfg {
   static constexpr int BLOCK_BYTES = 128 * 64 * 2;   // 128 rows x 64 columns, 128-byte swizzle
   static constexpr int TILE_BYTES = KBLK * BLOCK_BYTES;
   static constexpr int STAGES = (D == 128) ? 2 : 4;
-  static constexpr int LD_BYTES = 128 * 8;           // lse2[128] then Dl[128] of a query tile
+  static constexpr int SEED_BYTES = 128 * 16 * 2;    // one 128 x 16 bf16 seed operand
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
 
@@ -70,8 +78,9 @@ struct BwdCfg {
   static constexpr int KV_V_OFF = TILE_BYTES;
   static constexpr int KV_Q_OFF = 2 * TILE_BYTES;
   static constexpr int KV_DO_OFF = KV_Q_OFF + STAGES * TILE_BYTES;
-  static constexpr int KV_LD_OFF = KV_DO_OFF + STAGES * TILE_BYTES;
-  static constexpr int KV_BAR_OFF = KV_LD_OFF + STAGES * LD_BYTES;
+  static constexpr int KV_SEED_OFF = KV_DO_OFF + STAGES * TILE_BYTES;      // per stage: -lse seed, -Dl seed
+  static constexpr int KV_ONES_OFF = KV_SEED_OFF + STAGES * 2 * SEED_BYTES;  // 128 x 16: ones in columns 0-2
+  static constexpr int KV_BAR_OFF = KV_ONES_OFF + SEED_BYTES;
   // kv_full, full[S], empty[S], s_full, dp_full, p_full[2], ds_full[2], dv_done, dk_done, acc_done, drain
   static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 10;
   static constexpr int KV_MISC_OFF = KV_BAR_OFF + KV_NUM_BARS * 8;
@@ -107,12 +116,35 @@ enum : unsigned {
 // K-step kk (16 values = 8 columns) therefore starts at this column.
 __device__ __forceinline__ uint32_t bwd_packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
+// Byte offset of element (row r, k) in a 128 x 16 bf16 K-major operand without
+// swizzle: 8 x 8 core matrices of 128 contiguous bytes, 128 bytes apart along
+// K (LBO) and 256 bytes apart along the rows (SBO).
+__host__ __device__ constexpr int bwd_seed_offset(int r, int k) {
+  return (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// v as the sum of three bf16 values (hi + mid + lo = v to about 2^-24 |v|),
+// packed as the first three of eight bf16 in a 16-byte row chunk.
+__device__ __forceinline__ uint4 bwd_seed_row(float v) {
+  if (!(fabsf(v) < CUDART_INF_F)) {  // -inf (a row that sees no key): the first part carries it
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    return make_uint4(hi, 0u, 0u, 0u);
+  }
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  return make_uint4(__bfloat16_as_ushort(hi) | (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16),
+                    __bfloat16_as_ushort(lo), 0u, 0u);
+}
+
 // Per query row: lse2 = lse * log2(e) (+inf for a row that sees no key, so
 // that its P is 0) and Dl = sum_t dO_t O_t in fp32 over the bf16 inputs.
 // One 16-byte chunk per thread; the D/8 threads of a row reduce by shuffles.
 template <int D>
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dl,
+                                uint8_t* __restrict__ seed_l, uint8_t* __restrict__ seed_d, float scale,
                                 long long heads, int Nq, int Nq_pad) {
   constexpr int TPR = D / 8;
   const long long n = heads * Nq_pad * TPR;
@@ -145,8 +177,18 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_
         const float l = lse[(size_t)hh * Nq + i];
         l2 = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
       }
+      const float d = i < Nq ? acc : 0.f;
       lse2[(size_t)hh * Nq_pad + i] = l2;
-      dl[(size_t)hh * Nq_pad + i] = i < Nq ? acc : 0.f;
+      dl[(size_t)hh * Nq_pad + i] = d;
+      // Seeds of the dK/dV kernel: -lse/scale, so that (S^T + seed) scale
+      // log2 e = S^T scale log2 e - lse2 (-inf for rows whose P is 0), and -Dl.
+      const size_t tile = (size_t)hh * (Nq_pad / 128) + i / 128;
+      const int r = i & 127;
+      const float vl = l2 == CUDART_INF_F ? -CUDART_INF_F : -l2 / (scale * 1.4426950408889634f);
+      *reinterpret_cast<uint4*>(seed_l + tile * 4096 + bwd_seed_offset(r, 0)) = bwd_seed_row(vl);
+      *reinterpret_cast<uint4*>(seed_l + tile * 4096 + bwd_seed_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(seed_d + tile * 4096 + bwd_seed_offset(r, 0)) = bwd_seed_row(-d);
+      *reinterpret_cast<uint4*>(seed_d + tile * 4096 + bwd_seed_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 }
@@ -186,7 +228,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = smem + C::KV_V_OFF;
   uint8_t* sQ = smem + C::KV_Q_OFF;
   uint8_t* sDO = smem + C::KV_DO_OFF;
-  uint8_t* sLD = smem + C::KV_LD_OFF;
+  uint8_t* sSEED = smem + C::KV_SEED_OFF;
+  uint8_t* sONES = smem + C::KV_ONES_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::KV_BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* full = bars + 1;
@@ -241,6 +284,13 @@ __global__ void __launch_bounds__(320, 1)
     tmem_alloc(tmem_holder, C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (threadIdx.x < 256) {  // the seed MMAs' A operand: rows of (1, 1, 1, 0, ..., 0)
+    const int r = threadIdx.x >> 1, khalf = threadIdx.x & 1;
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    *reinterpret_cast<uint4*>(sONES + bwd_seed_offset(r, 8 * khalf)) =
+        khalf == 0 ? make_uint4(one | (one << 16), one, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // read by the tensor core (async proxy)
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -263,14 +313,15 @@ __global__ void __launch_bounds__(320, 1)
         if (u > 0 && !mbar_wait(empty + s, (u - 1) & 1, a.status, kSiteBwdEmpty)) { *abort_flag = 1; break; }
         const int h = hkv * a.group + n / per_head;
         const int q0 = (qt0 + n % per_head) * 128;
-        mbar_arrive_expect_tx(full + s, 2 * C::TILE_BYTES + C::LD_BYTES);
+        mbar_arrive_expect_tx(full + s, 2 * C::TILE_BYTES + 2 * C::SEED_BYTES);
         for (int kb = 0; kb < C::KBLK; ++kb) {
           tma_load_3d(sQ + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, full + s, kb * 64, q0, b * a.Hq + h);
           tma_load_3d(sDO + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_do, full + s, kb * 64, q0, b * a.Hq + h);
         }
-        const size_t row0 = (size_t)(b * a.Hq + h) * a.Nq_pad + q0;
-        bulk_load(sLD + s * C::LD_BYTES, a.lse2 + row0, C::LD_BYTES / 2, full + s);
-        bulk_load(sLD + s * C::LD_BYTES + C::LD_BYTES / 2, a.dl + row0, C::LD_BYTES / 2, full + s);
+        const size_t tile = (size_t)(b * a.Hq + h) * (a.Nq_pad / 128) + q0 / 128;
+        bulk_load(sSEED + s * 2 * C::SEED_BYTES, a.seed_l + tile * C::SEED_BYTES, C::SEED_BYTES, full + s);
+        bulk_load(sSEED + s * 2 * C::SEED_BYTES + C::SEED_BYTES, a.seed_d + tile * C::SEED_BYTES, C::SEED_BYTES,
+                  full + s);
         issued = n + 1;
         if (*abort_flag) break;
       }
@@ -293,24 +344,30 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
         const uint32_t q_addr = smem_u32(sQ + s * C::TILE_BYTES);
         const uint32_t do_addr = smem_u32(sDO + s * C::TILE_BYTES);
-        // S^T = K Q^T overwrites P^T of the previous step (read by its dV MMAs).
+        const uint32_t seed_addr = smem_u32(sSEED + s * 2 * C::SEED_BYTES);
+        const uint64_t ones_desc = smem_desc_noswizzle(smem_u32(sONES), 128, 256);
+        // S^T = -lse/scale (seed MMA) + K Q^T; it overwrites P^T of the
+        // previous step (read by its dV MMAs).
         if (n > 0 && !(ok = mbar_wait(dv_done, (n - 1) & 1, a.status, kSiteBwdDvDone))) break;
         tc_fence_after_sync();
+        umma_ss(tmem + C::T_ST, ones_desc, smem_desc_noswizzle(seed_addr, 128, 256), idesc_ss, 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
           umma_ss(tmem + C::T_ST, smem_desc_sw128(k_addr + off, 16, 1024), smem_desc_sw128(q_addr + off, 16, 1024),
-                  idesc_ss, kk > 0 ? 1u : 0u);
+                  idesc_ss, 1u);
         }
         umma_commit(s_full);
-        // dP^T = V dO^T overwrites dS^T of the previous step (read by its dK MMAs).
+        // dP^T = -Dl (seed MMA) + V dO^T; it overwrites dS^T of the previous
+        // step (read by its dK MMAs).
         if (n > 0 && !(ok = mbar_wait(dk_done, (n - 1) & 1, a.status, kSiteBwdDkDone))) break;
         tc_fence_after_sync();
+        umma_ss(tmem + C::T_DPT, ones_desc, smem_desc_noswizzle(seed_addr + C::SEED_BYTES, 128, 256), idesc_ss, 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
           umma_ss(tmem + C::T_DPT, smem_desc_sw128(v_addr + off, 16, 1024),
-                  smem_desc_sw128(do_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+                  smem_desc_sw128(do_addr + off, 16, 1024), idesc_ss, 1u);
         }
         umma_commit(dp_full);
         // dV += P^T dO, one half of the queries as soon as its warpgroup wrote P^T.
@@ -361,16 +418,11 @@ __global__ void __launch_bounds__(320, 1)
       const int s = n % C::STAGES;
       const int q0 = (qt0 + n % per_head) * 128;
       if (!(ok = mbar_wait(s_full, n & 1, a.status, kSiteBwdSFull))) break;
-      // (lse2, Dl) of this stage arrived by bulk copy: observe its barrier
-      // here too (already complete) so the copy's writes are visible.
-      if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
       tc_fence_after_sync();
-      // lse2 and Dl of this half's 64 query columns, four per 16-byte load (broadcasts)
-      const uint32_t lsp = smem_u32(sLD + s * C::LD_BYTES) + 256 * g, dlp = lsp + C::LD_BYTES / 2;
       // query q0 + 64g + c sees key kj iff c >= kj - causal_offset - q0 - 64g
       const bool need_mask = a.causal && key0 + 127 > q0 + 64 * g + a.causal_offset;
       const int cmin = kj - a.causal_offset - q0 - 64 * g;
-      // ---- phase 1: P^T = exp2(S^T scale log2 e - lse2), kept in fp32 for phase 2
+      // ---- phase 1: P^T = exp2((S^T - lse/scale) scale log2 e), kept in fp32 for phase 2
       float p[64];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
@@ -379,14 +431,11 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         tmem_reg_fence(sr);
         uint32_t pk[16];
-        float4 L;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
-          if ((i & 1) == 0) L = lds_f4(lsp + 4 * c);  // lse2 of columns c .. c+3
-          const float l0 = (i & 1) ? L.z : L.x, l1 = (i & 1) ? L.w : L.y;
           float x0, x1;
-          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, -l0, -l1);
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, 0.f, 0.f);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (need_mask) {
             p0 = c < cmin ? 0.f : p0;
@@ -401,7 +450,7 @@ __global__ void __launch_bounds__(320, 1)
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(p_full + g);
-      // ---- phase 2: dS^T = P^T (dP^T - Dl)
+      // ---- phase 2: dS^T = P^T (dP^T - Dl), the accumulator already holding dP^T - Dl
       if (!(ok = mbar_wait(dp_full, n & 1, a.status, kSiteBwdDpFull))) break;
       tc_fence_after_sync();
 #pragma unroll
@@ -411,15 +460,10 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         tmem_reg_fence(dr);
         uint32_t dk[16];
-        float4 L;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 32 * pass + 2 * i;
-          if ((i & 1) == 0) L = lds_f4(dlp + 4 * c);  // Dl of columns c .. c+3
-          const float e0 = (i & 1) ? L.z : L.x, e1 = (i & 1) ? L.w : L.y;
-          float d0, d1;
-          fma2(d0, d1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), 1.f, 1.f, -e0, -e1);
-          dk[i] = pack_bf16x2(p[c] * d0, p[c + 1] * d1);
+          dk[i] = pack_bf16x2(p[c] * __uint_as_float(dr[2 * i]), p[c + 1] * __uint_as_float(dr[2 * i + 1]));
         }
         tmem_st16(tDPT + 16 * pass, dk);
       }

@@ -125,8 +125,9 @@ ATTN_API attn_status attn_fwd_rope(const void* q, const void* k, const void* v, 
                                    float rope_base, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Workspace bytes attn_bwd needs: 8 bytes per query row (two fp32 values), each head's rows
- * padded to a multiple of 128. 0 for arguments attn_bwd would reject.
+ * Workspace bytes attn_bwd needs: 72 bytes per query row (two fp32 values and
+ * two 32-byte operand rows), each head's rows padded to a multiple of 128.
+ * 0 for arguments attn_bwd would reject.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
 

@@ -175,11 +175,11 @@ def test_bwd_argument_checks(lib):
     assert f(dq=FAKE + 8) == binding.ERR_INVALID_ARG      # not 16-byte aligned
     assert f(ws=0x100010) == binding.ERR_INVALID_ARG      # not 256-byte aligned
     assert f(ws=None) == binding.ERR_INVALID_ARG
-    assert f(wsb=4 * 256 * 8 - 1) == binding.ERR_INVALID_ARG
+    assert f(wsb=4 * 256 * 72 - 1) == binding.ERR_INVALID_ARG
     assert f(d=96) == binding.ERR_UNSUPPORTED
-    # (lse2, Dl) per query row, each head padded to 128 rows
-    assert lib.attn_bwd_workspace_size(1, 4, 200) == 4 * 256 * 8
-    assert lib.attn_bwd_workspace_size(2, 3, 128) == 6 * 128 * 8
+    # per query row: lse2 and Dl (fp32) and two 32-byte seed rows; heads padded to 128 rows
+    assert lib.attn_bwd_workspace_size(1, 4, 200) == 4 * 256 * 72
+    assert lib.attn_bwd_workspace_size(2, 3, 128) == 6 * 128 * 72
     assert lib.attn_bwd_workspace_size(0, 4, 200) == 0
 
 
