@@ -23,7 +23,8 @@ def _declared_functions():
     names = []
     for h in os.listdir(os.path.join(ROOT, "include")):
         if h.endswith(".h"):
-            text = open(os.path.join(ROOT, "include", h)).read()
+            with open(os.path.join(ROOT, "include", h)) as f:
+                text = f.read()
             names += re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
     return sorted(set(names))
 
