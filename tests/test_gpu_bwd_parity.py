@@ -116,14 +116,17 @@ def _full_size(w, q_samples, key_check):
     key_check(q, k, v, do, dk, dv)
     # sum_j dK_j = 0 and sum_j dV_j = sum over the group's rows of dO, at any
     # size. Each row carries independent rounding errors of order u |row|, so
-    # the sum's error grows like their root-sum-square (bounded at 4 u times it).
+    # the sum's error grows like their root-sum-square: 4 u times it for the
+    # bf16 rounding of P, dS and the outputs, and as much again for Dl, whose
+    # error (from the bf16 forward output) enters sum_j dK_j as
+    # scale sum_i dDl_i q_i, a random walk of the same order over the rows.
     G = w.Hq // w.Hkv
     for name, g, want in (("dk", dk, torch.zeros(w.B, w.Hkv, w.d, device=DEV, dtype=torch.float64)),
                           ("dv", dv, do.double().reshape(w.B, w.Hkv, G * w.Nq, w.d).sum(dim=2))):
         rss = g.double().pow(2).sum(dim=2).sqrt()
         dev = (g.double().sum(dim=2) - want).abs()
-        print(w.name, name, "sum invariant: worst deviation / (4u rss)", (dev / (4 * BF16_U * rss)).max().item())
-        assert (dev <= 4 * BF16_U * rss).all(), name
+        print(w.name, name, "sum invariant: worst deviation / (8u rss)", (dev / (8 * BF16_U * rss)).max().item())
+        assert (dev <= 8 * BF16_U * rss).all(), name
 
 
 def test_causal_mha_4096_sampled():
