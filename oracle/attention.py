@@ -4,8 +4,7 @@ Only the tests, the smoke check and the benchmark's CPU arms import this file.
 Source key ([MG-A], [MG-B], [AUT], [IMR], [PW]) is spelled out in
 ``oracle/__init__.py``; each function names the passage it follows.
 
-Readings taken where the pages are silent (each one is listed with its reason
-in the design notes):
+Readings taken where the pages are silent:
   * the score scale is applied before the mask; masked scores are -inf;
   * causal with Nq != Nk aligns the last query with the last key: query i sees
     key j iff j <= i + (Nk - Nq) (equal to the pages' j <= i when Nq == Nk);
@@ -246,14 +245,29 @@ def rope_rotate(x, positions, base: float = 10000.0):
 
 
 def round_to_bf16(x):
-    """fp64 -> nearest bf16 value (ties to even), returned as fp64."""
+    """fp64 -> nearest bf16 value (ties to even), returned as fp64.
+
+    One rounding, straight from fp64: bf16 keeps 8 significant bits, so in the
+    binade [2^(e-1), 2^e) of |x| its values are the integer multiples of
+    2^(e-8) (below the smallest normal, 2^-126, the spacing stays 2^-133). The
+    result is the multiple nearest |x|; an exact half goes to the even
+    multiple. Magnitudes that round to 2^128 or more become infinite (the
+    largest finite bf16 is (2 - 2^-7) 2^127); NaN, +-inf and +-0 pass through.
+    """
     x = np.asarray(x, dtype=np.float64)
-    f = x.astype(np.float32)
-    bits = f.view(np.uint32).astype(np.uint64)
-    lsb = (bits >> 16) & 1
-    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
-    out = rounded.astype(np.uint32).view(np.float32).astype(np.float64)
-    return np.where(np.isfinite(f), out, f.astype(np.float64))
+    out = np.array(x, dtype=np.float64, copy=True)
+    fin = np.isfinite(x) & (x != 0.0)
+    ax = np.abs(x[fin])
+    _, e = np.frexp(ax)                          # ax = frac * 2^e, 0.5 <= frac < 1
+    spacing = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    t = ax / spacing                             # exact: a power-of-two scaling
+    n = np.floor(t)
+    rem = t - n                                  # exact fraction in [0, 1)
+    up = (rem > 0.5) | ((rem == 0.5) & (np.fmod(n, 2.0) == 1.0))
+    mag = (n + up) * spacing
+    mag = np.where(mag >= 2.0 ** 128, np.inf, mag)
+    out[fin] = np.copysign(mag, x[fin])
+    return out
 
 
 def attention_forward_rope(q, k, v, scale: float, causal: bool, base: float = 10000.0, window: int = 0):

@@ -530,14 +530,87 @@ def test_rope_attention_matches_rotating_by_hand_and_rounding():
     qr = q.copy()
     qr[..., 0::2] = q[..., 0::2] * np.cos(theta_q) - q[..., 1::2] * np.sin(theta_q)
     qr[..., 1::2] = q[..., 0::2] * np.sin(theta_q) + q[..., 1::2] * np.cos(theta_q)
-    qr = torch.from_numpy(qr).to(torch.bfloat16).double().numpy()  # RNE to bf16 by torch
-    kr = torch.from_numpy(rope_rotate(k, np.arange(Nk))).to(torch.bfloat16).double().numpy()
+    qr = _nearest_bf16_by_table(qr)  # the rounding is pinned on its own below
+    kr = _nearest_bf16_by_table(rope_rotate(k, np.arange(Nk)))
     o2, lse2 = attention_forward(qr, kr, v, 0.3, True)
     np.testing.assert_array_equal(o, o2)
     np.testing.assert_array_equal(lse, lse2)
-    # the rounding helper agrees with torch's bf16 conversion bit for bit
-    x = rng.standard_normal(10000) * 10 ** rng.uniform(-3, 3, 10000)
-    np.testing.assert_array_equal(round_to_bf16(x), torch.from_numpy(x).float().to(torch.bfloat16).double().numpy())
+
+
+# --- rounding fp64 -> bf16 (the RoPE reading: rotated operands are rounded once, to nearest, ties to even)
+
+def _bf16_table():
+    """Every finite non-negative bf16 value in increasing order, from the bit
+    patterns (bf16_bits_to_f64 is pinned against all 65 536 patterns)."""
+    vals = bf16_bits_to_f64(np.arange(0, 0x7F80, dtype=np.uint16))
+    assert np.all(np.diff(vals) > 0)
+    return vals
+
+
+def _nearest_bf16_by_table(x):
+    """Brute force: look |x| up between its two bf16 neighbours, pick the
+    nearer one, on a tie the one whose bit pattern is even."""
+    x = np.asarray(x, dtype=np.float64)
+    tab = _bf16_table()
+    ax = np.abs(x)
+    i = np.clip(np.searchsorted(tab, ax, side="right") - 1, 0, tab.size - 1)  # tab[i] <= ax
+    lo = tab[i]
+    hi = np.where(i + 1 < tab.size, tab[np.minimum(i + 1, tab.size - 1)], np.inf)
+    d_lo, d_hi = ax - lo, hi - ax
+    # above the largest finite value the upper neighbour is +inf at distance "one more step"
+    top = i + 1 >= tab.size
+    d_hi = np.where(top, (tab[-1] - tab[-2]) - d_lo, d_hi)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (i % 2 == 1))
+    return np.copysign(np.where(pick_hi, hi, lo), x)
+
+
+def test_round_to_bf16_hand_cases():
+    """Cases fixed by round-to-nearest-even alone (no conversion library in between):
+    bf16 keeps 8 significant bits, so next to 1 its spacing is 2^-7."""
+    u = 2.0 ** -7
+    cases = [
+        (1 + u / 2 + 2.0 ** -30, 1 + u),  # just above the midpoint: up (a detour through fp32 gives 1.0)
+        (1 + u / 2, 1.0),                 # the midpoint: to the even neighbour 1.0
+        (1 + u / 2 - 2.0 ** -40, 1.0),    # just below: down
+        (1 + 3 * u / 2, 1 + 2 * u),       # midpoint between odd 1+u and even 1+2u: up to even
+        (1 + u, 1 + u),                   # representable values stay
+        (2 - u / 4, 2.0),                 # rounding up carries into the next binade
+        (0.0, 0.0),
+    ]
+    for scale in (1.0, -1.0, 2.0 ** -100, -(2.0 ** 90), 2.0 ** 120):
+        for x, want in cases:
+            got = round_to_bf16(np.array([x * scale]))[0]
+            assert got == want * scale, (x, scale, got, want * scale)
+
+
+def test_round_to_bf16_extremes():
+    big = (2 - 2.0 ** -7) * 2.0 ** 127  # largest finite bf16
+    half_step = 2.0 ** (127 - 8)
+    tiny = 2.0 ** -133                  # smallest subnormal bf16
+    x = np.array([big, big + half_step * 0.99, big + half_step, -(big + half_step), 1.5 * tiny, 2.5 * tiny,
+                  0.5 * tiny, 0.5 * tiny * (1 + 2.0 ** -20), np.inf, -np.inf, 1e-300])
+    want = np.array([big, big, np.inf, -np.inf, 2 * tiny, 2 * tiny, 0.0, tiny, np.inf, -np.inf, 0.0])
+    np.testing.assert_array_equal(round_to_bf16(x), want)
+    assert np.isnan(round_to_bf16(np.array([np.nan]))[0])
+    assert np.signbit(round_to_bf16(np.array([-1e-300]))[0])
+
+
+def test_round_to_bf16_matches_brute_force_between_every_pair_of_neighbours():
+    """For every pair of adjacent finite bf16 values: points at 1/4, just below,
+    at, and just above the midpoint, and at 3/4 of the gap, both signs."""
+    tab = _bf16_table()
+    lo, hi = tab[:-1], tab[1:]
+    gap = hi - lo
+    pts = [lo + gap * f for f in (0.25, 0.75)]
+    mid = lo + gap / 2
+    pts += [mid, np.nextafter(mid, -np.inf), np.nextafter(mid, np.inf)]
+    x = np.concatenate(pts)
+    x = np.concatenate([x, -x])
+    np.testing.assert_array_equal(round_to_bf16(x), _nearest_bf16_by_table(x))
+    # and random magnitudes over the whole range
+    rng = np.random.default_rng(73)
+    y = rng.standard_normal(200000) * 2.0 ** rng.uniform(-140, 127, 200000)
+    np.testing.assert_array_equal(round_to_bf16(y), _nearest_bf16_by_table(y))
 
 
 # ---------------------------------------------------------------- backward pass
