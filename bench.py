@@ -1,26 +1,31 @@
-"""Benchmark: exact causal attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
+"""Benchmark: exact attention prefill (TFLOP/s) and KV-cache decode (GB/s) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--prefill NAME] [--only prefill|decode|paged|window|backward|rope]
-                    [--no-cpu-baseline] [--no-e2e]
+                    [--prefill NAME] [--only PART] [--no-cpu-baseline] [--no-e2e]
 
 One step = one pass of the whole hot path over synthetic bf16 inputs that are
-already resident in device memory: a causal GQA prefill (B=1, Hq=64, Hkv=8,
-N=16384, d=128), a decode step (B=16, Hq=32, Hkv=8, d=128, cache lengths
-uniform on [1024, 8192]), the same decode over a paged cache (64-token
-pages) with the new token appended, the prefill again with a 4096-key
-causal sliding window, and the backward pass of the causal prefill (dQ, dK,
-dV from the o and lse that step's prefill wrote and a seeded dO) and the prefill
-with rotary position embedding (base 10000) in a second loop. L2 is flushed (a 256 MiB write) before each
-of the two launches, outside their CUDA-event brackets, followed by a 256 MiB
-read so the timed kernel does not pay for writing back the flush's dirty lines.
+already resident in device memory, one timed launch per part:
+  prefill         causal GQA prefill B=1 Hq=64 Hkv=8 N=16384 d=128 (the line's value)
+  decode          B=16 Hq=32 Hkv=8 d=128, cache lengths uniform on [1024, 8192]
+  c1_single_head  B=1 H=1 N=128 d=64, non-causal
+  c2_mha_d64      B=4 H=12 N=2048 d=64, non-causal
+  c3_causal_mha   B=2 H=32 N=4096 d=128, causal
+  window          the causal GQA prefill with a 4096-key sliding window
+  paged           the decode over a paged cache (64-token pages), new token appended
+and, in a second loop, the backward pass of the causal GQA prefill (dQ, dK, dV
+from the o and lse its prefill wrote and a seeded dO) and that prefill with
+rotary position embedding (base 10000). L2 is flushed before every timed
+launch, outside its CUDA-event bracket: a 256 MiB write, then a 256 MiB read
+so the timed kernel does not pay for writing back the flush's dirty lines.
 Prints one JSON line.
 
-``value`` is prefill TFLOP/s (4*B*Hq*Nq*Nk*d, halved for causal) over the
-prefill launches; the decode result sits in ``decode`` (GB/s of the cache
-rows actually read, sum(seqlens)*Hkv*d*2*2 bytes, plus q, o and lse).
-Under torchrun every rank runs the same workload (replicas; weak scaling)
-and rank 0 prints the aggregate over the max-over-ranks time.
+``value`` is the causal GQA prefill's TFLOP/s (4*B*Hq*Nq*Nk*d, halved for
+causal); every other part has its own block with its own roofline (decode:
+GB/s of the cache rows actually read, sum(seqlens)*Hkv*d*2*2 bytes, plus q, o
+and lse). Each roofline gives the fraction of the measured peak and of the
+nominal B300 peak. Under torchrun every rank runs the same workload
+(replicas; weak scaling) and rank 0 prints the aggregate over the
+max-over-ranks time.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
 of the same workload per step, on the host cores (rank 0 only).
@@ -47,6 +52,13 @@ from exact_scaled_dot_03_b300 import workloads as W  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (bf16, causal) and decode GB/s; % of B300 roofline"
 PREFILL = {w.name: w for w in W.PREFILL_WORKLOADS}
+# The other prefill workloads, each timed as its own part of the step.
+EXTRA_PREFILL = (("c1_single_head", W.SINGLE_HEAD), ("c2_mha_d64", W.MHA_2048),
+                 ("c3_causal_mha", W.CAUSAL_MHA_4096))
+# Nominal B300 figures the stated targets are written against (dense bf16 tensor
+# rate, HBM3e bandwidth): every roofline block also reports its fraction of these.
+SPEC_BF16_TFLOPS = 2250.0
+SPEC_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 256 << 20
 WINDOW = 4096  # local-window width of the sliding-window prefill measured beside the full one
 
@@ -66,7 +78,35 @@ def measured_peaks():
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
-    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+    # Not a measurement of this GPU: an earlier B300 reading, used only when the
+    # measured file is missing, and labelled as such in every block.
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "FALLBACK (not measured on this GPU)"}
+
+
+def tensor_roof(achieved, peaks, flops, kernel, traffic=None, **extra):
+    """Roofline block of a tensor-bound kernel: TFLOP/s against the measured
+    cuBLAS bf16 burst peak and against the nominal dense bf16 rate."""
+    r = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+         "frac": achieved / peaks["bf16_tflops"],
+         "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                               if peaks.get("bf16_tflops_sustained") else None),
+         "frac_of_spec": achieved / SPEC_BF16_TFLOPS, "spec_peak": SPEC_BF16_TFLOPS,
+         "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)", "traffic": traffic,
+         "algorithmic_flops_per_launch": flops, "kernel": kernel}
+    r.update(extra)
+    return r
+
+
+def hbm_roof(achieved, peaks, nbytes, kernel, traffic=None, **extra):
+    """Roofline block of an HBM-bound kernel: GB/s against the measured copy
+    bandwidth and against the nominal HBM3e bandwidth."""
+    r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": achieved / peaks["hbm_gbs"], "frac_of_spec": achieved / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
+         "peak_source": f"{peaks['source']} copy bandwidth", "traffic": traffic,
+         "algorithmic_bytes_per_launch": nbytes, "kernel": kernel}
+    r.update(extra)
+    return r
 
 
 def kernel_source_hash(files):
@@ -269,15 +309,15 @@ def run_ours(args, w, wd):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    do_pre = args.only in (None, "prefill")
-    do_dec = args.only in (None, "decode")
-    do_pag = args.only in (None, "paged")
-    do_win = args.only in (None, "window")
-    do_bwd = args.only in (None, "backward")
-    do_rope = args.only in (None, "rope")
+    on = lambda name: args.only in (None, name)  # noqa: E731
+    do_pre, do_dec, do_pag, do_win, do_bwd, do_rope = (on(n) for n in
+                                                      ("prefill", "decode", "paged", "window", "backward", "rope"))
+    extra = [(name, wx) for name, wx in EXTRA_PREFILL if on(name)]
 
     parts = []  # (name, launch function)
-    kernels = {"prefill": 1, "decode": 1, "window": 1, "paged": 1, "backward": 3, "rope": 3}  # our launches per call
+    # our kernel launches per call
+    kernels = {"prefill": 1, "decode": 1, "window": 1, "paged": 1, "backward": 3, "rope": 3,
+               **{name: 1 for name, _ in EXTRA_PREFILL}}
     if do_pre or do_bwd or do_rope:
         q_h, k_h, v_h = W.prefill_inputs(w)
         q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
@@ -293,6 +333,12 @@ def run_ours(args, w, wd):
         ws = binding.decode_workspace(wd.B, wd.Hq, wd.Hkv, wd.Lmax, wd.d, device=dev)
         parts.append(("decode", lambda: binding.decode(dq, kc, vc, sl, scale=wd.scale, workspace=ws, out=do,
                                                        lse=dlse)))
+    for name, wx in extra:
+        xq, xk, xv = (t.to(dev) for t in W.prefill_inputs(wx))
+        xo = torch.empty_like(xq)
+        xl = torch.empty(wx.B, wx.Hq, wx.Nq, dtype=torch.float32, device=dev)
+        parts.append((name, lambda wx=wx, xq=xq, xk=xk, xv=xv, xo=xo, xl=xl:
+                      binding.fwd(xq, xk, xv, causal=wx.causal, scale=wx.scale, out=xo, lse=xl)))
     if do_win:
         ww = W.CAUSAL_GQA_16384
         if not do_pre:
@@ -395,104 +441,85 @@ def run_ours(args, w, wd):
 
     tot = max_over_ranks({name: sum(v) for name, v in ms.items()}, dev)
     peaks = measured_peaks()
+    mean_s = lambda name: statistics.mean(ms[name]) / 1e3  # noqa: E731  (seconds per launch)
 
-    roofline = dec_block = None
-    value = unit = None
+    blocks = {}  # name -> block, in the order they are printed
+    headline = None
     if do_pre:
         flops = w.flops()
-        value = job_rate(flops, args.steps, world, tot["prefill"]) / 1e12
-        unit = "TFLOP/s"
-        achieved = flops / (statistics.mean(ms["prefill"]) / 1e3) / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"],
-                    "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
-                                          if peaks.get("bf16_tflops_sustained") else None),
-                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                    "traffic": profiled_traffic("attn_fwd_kernel_causal_gqa_traffic.txt",
-                                                ("fwd_kernel.cuh", "ptx.cuh")),
-                    "algorithmic_flops_per_launch": flops, "kernel": "attn_fwd_kernel<128>"}
+        blocks["prefill"] = {
+            "metric": "causal prefill TFLOP/s", "workload": w.name,
+            "value": job_rate(flops, args.steps, world, tot["prefill"]) / 1e12, "unit": "TFLOP/s",
+            "ms": tot["prefill"] / args.steps,
+            "roofline": tensor_roof(flops / mean_s("prefill") / 1e12, peaks, flops, "attn_fwd_kernel<128>",
+                                    profiled_traffic("attn_fwd_kernel_causal_gqa_traffic.txt",
+                                                     ("fwd_kernel.cuh", "ptx.cuh")))}
     if do_dec:
         dec_bytes = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
-        dec_value = job_rate(dec_bytes, args.steps, world, tot["decode"]) / 1e9
-        dec_achieved = dec_bytes / (statistics.mean(ms["decode"]) / 1e3) / 1e9
-        dec_roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": dec_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
-                    "traffic": profiled_traffic("attn_decode_kernel_gqa_traffic.txt",
-                                                ("decode_kernel.cuh", "ptx.cuh")),
-                    "algorithmic_bytes_per_launch": dec_bytes, "kernel": "attn_decode_kernel<128,4>"}
-        dec_block = {"metric": "decode GB/s (cache rows read + q/o/lse)", "value": dec_value, "unit": "GB/s",
-                     "ms": tot["decode"] / args.steps, "roofline": dec_roof}
-        if not do_pre:   # decode alone: its numbers are the line's
-            value, unit, roofline = dec_value, "GB/s", dec_roof
-    win_block = None
+        blocks["decode"] = {
+            "metric": "decode GB/s (cache rows read + q/o/lse)", "workload": wd.name,
+            "value": job_rate(dec_bytes, args.steps, world, tot["decode"]) / 1e9, "unit": "GB/s",
+            "ms": tot["decode"] / args.steps,
+            "roofline": hbm_roof(dec_bytes / mean_s("decode") / 1e9, peaks, dec_bytes, "attn_decode_kernel<128,4>",
+                                 profiled_traffic("attn_decode_kernel_gqa_traffic.txt",
+                                                  ("decode_kernel.cuh", "ptx.cuh")))}
+    for name, wx in extra:
+        f = wx.flops()
+        blk = {"metric": f"{'causal ' if wx.causal else ''}prefill TFLOP/s", "workload": wx.name,
+               "value": job_rate(f, args.steps, world, tot[name]) / 1e12, "unit": "TFLOP/s",
+               "ms": tot[name] / args.steps, "us_per_launch": 1e6 * mean_s(name),
+               "roofline": tensor_roof(f / mean_s(name) / 1e12, peaks, f, f"attn_fwd_kernel<{wx.d}>")}
+        if name == "c1_single_head":
+            blk["note"] = "one CTA: latency-bound by construction; the fraction is reported, not a target"
+        blocks[name] = blk
     if do_win:
         # FLOPs of the pairs that are actually visible: row i sees min(i+1, WINDOW) keys
         pairs = sum(min(i + 1, WINDOW) for i in range(ww.Nq))
         win_flops = 4.0 * ww.B * ww.Hq * ww.d * pairs
-        win_value = job_rate(win_flops, args.steps, world, tot["window"]) / 1e12
-        win_achieved = win_flops / (statistics.mean(ms["window"]) / 1e3) / 1e12
-        win_roof = {"bound": "tensor", "achieved": win_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": win_achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                    "traffic": None, "algorithmic_flops_per_launch": win_flops,
-                    "kernel": "attn_fwd_kernel<128, window>"}
-        win_block = {"metric": "causal sliding-window prefill TFLOP/s (visible pairs only)",
-                     "workload": f"{ww.name}_window{WINDOW}", "value": win_value, "unit": "TFLOP/s",
-                     "ms": tot["window"] / args.steps, "roofline": win_roof}
-        if not (do_pre or do_dec or do_pag):
-            value, unit, roofline = win_value, "TFLOP/s", win_roof
-    pag_block = None
+        blocks["prefill_window"] = {
+            "metric": "causal sliding-window prefill TFLOP/s (visible pairs only)",
+            "workload": f"{ww.name}_window{WINDOW}",
+            "value": job_rate(win_flops, args.steps, world, tot["window"]) / 1e12, "unit": "TFLOP/s",
+            "ms": tot["window"] / args.steps,
+            "roofline": tensor_roof(win_flops / mean_s("window") / 1e12, peaks, win_flops,
+                                    "attn_fwd_kernel<128, window>")}
     if do_pag:
         pag_bytes = ((int(psl_h.sum()) + wp.B) * wp.Hkv * wp.d * 2 * 2 + 2 * wp.B * wp.Hq * wp.d * 2
                      + 4 * wp.B * wp.Hq + 2 * wp.B * wp.Hkv * wp.d * 2 * 2)
-        pag_value = job_rate(pag_bytes, args.steps, world, tot["paged"]) / 1e9
-        pag_achieved = pag_bytes / (statistics.mean(ms["paged"]) / 1e3) / 1e9
-        pag_roof = {"bound": "hbm", "achieved": pag_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": pag_achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy bandwidth",
-                    "traffic": None, "algorithmic_bytes_per_launch": pag_bytes,
-                    "kernel": "attn_decode_kernel<128,4> (paged, append)"}
-        pag_block = {"metric": "paged decode + append GB/s (cache rows read incl. the new token, q/o/lse, "
-                               "appended rows read and written)", "workload": wp.name, "value": pag_value,
-                     "unit": "GB/s", "ms": tot["paged"] / args.steps, "roofline": pag_roof}
-        if not do_pre and not do_dec:
-            value, unit, roofline = pag_value, "GB/s", pag_roof
-
-    bwd_block = None
+        blocks["decode_paged"] = {
+            "metric": "paged decode + append GB/s (cache rows read incl. the new token, q/o/lse, "
+                      "appended rows read and written)", "workload": wp.name,
+            "value": job_rate(pag_bytes, args.steps, world, tot["paged"]) / 1e9, "unit": "GB/s",
+            "ms": tot["paged"] / args.steps,
+            "roofline": hbm_roof(pag_bytes / mean_s("paged") / 1e9, peaks, pag_bytes,
+                                 "attn_decode_kernel<128,4> (paged, append)")}
     if do_bwd:
         # The usual convention for the backward: 2.5x the forward's FLOPs (five
         # products of the forward's size: S, dP, dV, dK, dQ); the recomputation
         # of S and dP in the dQ kernel is not counted.
         bwd_flops = 2.5 * w.flops()
-        bwd_value = job_rate(bwd_flops, args.steps, world, tot["backward"]) / 1e12
-        bwd_achieved = bwd_flops / (statistics.mean(ms["backward"]) / 1e3) / 1e12
-        bwd_roof = {"bound": "tensor", "achieved": bwd_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": bwd_achieved / peaks["bf16_tflops"],
-                    "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                    "traffic": profiled_traffic("attn_bwd_causal_gqa_traffic.txt", ("bwd_kernel.cuh", "ptx.cuh")),
-                    "traffic_note": "DRAM bytes of one backward call (dK/dV + dQ kernels), from the ncu capture",
-                    "algorithmic_flops_per_launch": bwd_flops,
-                    "kernel": "bwd_prep_kernel<128> + attn_bwd_dkdv_kernel<128> + attn_bwd_dq_kernel<128>"}
-        bwd_block = {"metric": "causal attention backward TFLOP/s (2.5x forward FLOPs)", "workload": w.name,
-                     "value": bwd_value, "unit": "TFLOP/s", "ms": tot["backward"] / args.steps,
-                     "roofline": bwd_roof}
-        if not (do_pre or do_dec or do_pag or do_win):
-            value, unit, roofline = bwd_value, "TFLOP/s", bwd_roof
-
-    rope_block = None
+        blocks["backward"] = {
+            "metric": "causal attention backward TFLOP/s (2.5x forward FLOPs)", "workload": w.name,
+            "value": job_rate(bwd_flops, args.steps, world, tot["backward"]) / 1e12, "unit": "TFLOP/s",
+            "ms": tot["backward"] / args.steps,
+            "roofline": tensor_roof(bwd_flops / mean_s("backward") / 1e12, peaks, bwd_flops,
+                                    "bwd_prep_kernel<128> + attn_bwd_dkdv_kernel<128> + attn_bwd_dq_kernel<128>",
+                                    profiled_traffic("attn_bwd_causal_gqa_traffic.txt", ("bwd_kernel.cuh", "ptx.cuh")),
+                                    traffic_note="DRAM bytes of one backward call (dK/dV + dQ kernels), "
+                                                 "from the ncu capture")}
     if do_rope:
         # The pre-pass (table + rotated K) is inside the timed call; FLOPs are the prefill's.
         rflops = w.flops()
-        rope_value = job_rate(rflops, args.steps, world, tot["rope"]) / 1e12
-        rope_achieved = rflops / (statistics.mean(ms["rope"]) / 1e3) / 1e12
-        rope_roof = {"bound": "tensor", "achieved": rope_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": rope_achieved / peaks["bf16_tflops"],
-                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)", "traffic": None,
-                     "algorithmic_flops_per_launch": rflops,
-                     "kernel": "rope_table_kernel<128> + rope_k_kernel<128> + attn_fwd_kernel<128> (RoPE on Q)"}
-        rope_block = {"metric": "causal prefill with RoPE TFLOP/s (prefill FLOPs; table and K rotation included)",
-                      "workload": f"{w.name}_rope10000", "value": rope_value, "unit": "TFLOP/s",
-                      "ms": tot["rope"] / args.steps, "roofline": rope_roof}
-        if args.only == "rope":
-            value, unit, roofline = rope_value, "TFLOP/s", rope_roof
+        blocks["prefill_rope"] = {
+            "metric": "causal prefill with RoPE TFLOP/s (prefill FLOPs; table and K rotation included)",
+            "workload": f"{w.name}_rope10000",
+            "value": job_rate(rflops, args.steps, world, tot["rope"]) / 1e12, "unit": "TFLOP/s",
+            "ms": tot["rope"] / args.steps,
+            "roofline": tensor_roof(rflops / mean_s("rope") / 1e12, peaks, rflops,
+                                    "rope_table_kernel<128> + rope_k_kernel<128> + attn_fwd_kernel<128> (RoPE on Q)")}
+    # The line's own value: the causal GQA prefill, else the one part timed alone.
+    head_name = "prefill" if do_pre else next(iter(blocks))
+    headline = blocks.pop(head_name)
 
     e2e = None
     if do_pre and not args.no_e2e:   # every rank measures its own replica; rank 0 reports the aggregate
@@ -505,33 +532,25 @@ def run_ours(args, w, wd):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": sum(tot.values()) / args.steps,
+            "metric": METRIC, "value": headline["value"], "unit": headline["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(tot.values()) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16)",
-            "config": {"workload": (w.name if do_pre else wd.name if do_dec else W.DECODE_GQA_PAGED.name if do_pag
-                                    else f"{W.CAUSAL_GQA_16384.name}_window{WINDOW}" if do_win
-                                    else f"{w.name}_backward" if do_bwd else f"{w.name}_rope10000"),
+            "config": {"workload": headline["workload"],
                        "l2": "flushed before every timed launch: 256 MiB written, then 256 MiB read (no dirty lines left)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": headline["roofline"],
+            "peaks_used": {"bf16_tflops": peaks["bf16_tflops"], "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                           "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"],
+                           "spec_bf16_tflops": SPEC_BF16_TFLOPS, "spec_hbm_gbs": SPEC_HBM_GBS},
         }
-        if do_pre and do_dec:
-            line["config"]["decode_workload"] = wd.name
-        if do_pre:
-            line["prefill_ms"] = tot["prefill"] / args.steps
-        line["per_step_ms"] = {name: [round(x, 4) for x in v] for name, v in ms.items()}
-        if do_pre and do_dec:
-            line["decode"] = dec_block
-        if pag_block is not None and (do_pre or do_dec):
-            line["decode_paged"] = pag_block
-        if win_block is not None and (do_pre or do_dec or do_pag):
-            line["prefill_window"] = win_block
-        if bwd_block is not None and (do_pre or do_dec or do_pag or do_win):
-            line["backward"] = bwd_block
-        if rope_block is not None and args.only != "rope":
-            line["prefill_rope"] = rope_block
-        line.update({"roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
-                     "clocks": clocks, "wall_s_timed_region": t_wall})
+        if head_name == "prefill":
+            line["prefill_ms"] = headline["ms"]
+        # Short blocks first (the five workloads), the longer ones after.
+        line.update(blocks)
+        line.update({"cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
+                     "clocks": clocks, "wall_s_timed_region": t_wall,
+                     "median_ms": {name: round(statistics.median(v), 4) for name, v in ms.items()}})
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -582,7 +601,8 @@ def main():
     ap.add_argument("--prefill", default=W.CAUSAL_GQA_16384.name, choices=sorted(PREFILL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window", "backward", "rope"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged", "window", "backward", "rope",
+                                       *(name for name, _ in EXTRA_PREFILL)], default=None,
                     help="time one kernel alone (profiling); the JSON line then carries only its numbers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

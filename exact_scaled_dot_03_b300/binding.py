@@ -36,6 +36,7 @@ SIGNATURES = {
     "attn_kv_cache_bytes": (_u64, [_i64, _i64, _i64, _i64, _i]),
     "attn_version": (ctypes.c_char_p, []),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "attn_test_arm_stall": (_i, [_i]),
     "attn_decode_paged_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "attn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                _vp, _sz, _vp]),

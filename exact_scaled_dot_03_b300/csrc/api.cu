@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -34,14 +35,19 @@ int current_device() {
   return dev;
 }
 
+// Per-device values looked up once. Host threads may make their first calls
+// concurrently: the slots are atomics, and a lookup that two threads both make
+// stores the same value.
 unsigned* status_ptr(int dev) {
-  static unsigned* ptrs[kMaxDevices] = {};
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned*>(p);
+  static std::atomic<unsigned*> ptrs[kMaxDevices];
+  unsigned* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_attn_status) != cudaSuccess || a == nullptr) return nullptr;
+    p = static_cast<unsigned*>(a);
+    ptrs[dev].store(p, std::memory_order_release);
   }
-  return ptrs[dev];
+  return p;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -74,12 +80,25 @@ bool make_map(CUtensorMap* map, const void* base, int d, long long n, long long 
   return r == CUDA_SUCCESS;
 }
 
+// Raises a kernel's dynamic shared-memory limit once per device (setting it
+// twice from racing threads is harmless).
+using DevFlags = std::atomic<bool>[kMaxDevices];
 template <typename K>
-bool ensure_smem(K kernel, int bytes, int dev, bool* done) {
-  if (done[dev]) return true;
+bool ensure_smem(K kernel, int bytes, int dev, DevFlags& done) {
+  if (done[dev].load(std::memory_order_acquire)) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
-  done[dev] = true;
+  done[dev].store(true, std::memory_order_release);
   return true;
+}
+
+// Failure-detection test hook (attn_test_arm_stall): the kind of the kernel
+// whose next launch makes one wait stall, or 0.
+std::atomic<int> g_armed_stall{0};
+
+// 1 if the hook is armed for `kind` (and disarms it), else 0.
+int take_stall(int kind) {
+  int expected = kind;
+  return g_armed_stall.compare_exchange_strong(expected, 0) ? 1 : 0;
 }
 
 // o = 0 and lse = -inf for rows that see no key at all.
@@ -96,14 +115,14 @@ template <int D>
 attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream, int dev,
                        const float2* rope_cs = nullptr, int rope_pmin = 0, int rope_T = 0) {
-  static bool smem_set[kMaxDevices] = {};
+  static DevFlags smem_set;
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, 128) ||
       !make_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, 128) ||
       !make_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, 128))
     return ATTN_ERR_CUDA;
-  static bool smem_set_w[kMaxDevices] = {};
+  static DevFlags smem_set_w;
   if (!ensure_smem(attn_fwd_kernel<D, false>, C::SMEM_BYTES, dev, smem_set) ||
       !ensure_smem(attn_fwd_kernel<D, true>, C::SMEM_BYTES, dev, smem_set_w))
     return ATTN_ERR_CUDA;
@@ -126,6 +145,7 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = status_ptr(dev);
   if (a.status == nullptr) return ATTN_ERR_CUDA;
+  a.stall = take_stall(ATTN_TEST_STALL_PREFILL);
   dim3 grid(Hq, a.num_pairs, B);
   if (window > 0)
     attn_fwd_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
@@ -166,13 +186,13 @@ bool plan_decode(int B, int Hq, int Hkv, int Lmax, int d, DecodePlan* p) {
 }
 
 int sm_count(int dev) {
-  static int counts[kMaxDevices] = {};
-  if (counts[dev] == 0) {
-    int n = 0;
+  static std::atomic<int> counts[kMaxDevices];
+  int n = counts[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
-    counts[dev] = n;
+    counts[dev].store(n, std::memory_order_release);
   }
-  return counts[dev];
+  return n;
 }
 
 // Paged-cache layout and fused append for a decode launch (all null/zero for
@@ -188,7 +208,7 @@ template <int D, int GC>
 attn_status launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seqlens, void* o,
                           float* lse, int B, int Hq, int Hkv, int Lmax, float scale, void* ws,
                           const DecodePlan& plan, cudaStream_t stream, int dev, const DecodePaging& pg) {
-  static bool smem_set[kMaxDevices] = {};
+  static DevFlags smem_set;
   using C = DecCfg<D, GC>;
   CUtensorMap tk, tv;
   if (pg.block_table == nullptr) {
@@ -229,6 +249,7 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
   a.v_new = static_cast<const __nv_bfloat16*>(pg.v_new);
   a.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(kc));
   a.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(vc));
+  a.stall = take_stall(ATTN_TEST_STALL_DECODE);
   static_assert(C::TK == kDecTile && C::MIN_CHUNK == kDecMinChunk, "decode plan and kernel disagree");
   const int grid = sm_count(dev);  // persistent: one CTA per SM
   if (grid == 0) return ATTN_ERR_CUDA;
@@ -267,7 +288,7 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                        float* ws, int Nq_pad, cudaStream_t s, int dev) {
   using C = BwdCfg<D>;
-  static bool smem_kv[kMaxDevices] = {}, smem_q[kMaxDevices] = {};
+  static DevFlags smem_kv, smem_q;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, 128) ||
       !make_map(&tdo, dout, D, Nq, static_cast<long long>(B) * Hq, 128) ||
@@ -340,7 +361,9 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (Nk == 0) {
     const size_t rows = static_cast<size_t>(B) * Hq * Nq;
-    const int blocks = static_cast<int>(std::min<size_t>((rows * d + 255) / 256, 148 * 16));
+    const int sms = sm_count(dev);
+    if (sms == 0) return ATTN_ERR_CUDA;
+    const int blocks = static_cast<int>(std::min<size_t>((rows * d + 255) / 256, static_cast<size_t>(sms) * 16));
     fill_empty_kernel<<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(o), lse, rows, d);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
@@ -451,8 +474,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (Nq == 0 || Nk == 0) {
     // No query or no key: every gradient that exists is zero.
     const size_t qrows = static_cast<size_t>(B) * Hq * Nq, krows = static_cast<size_t>(B) * Hkv * Nk;
-    const int qb = static_cast<int>(std::min<size_t>((qrows * d + 255) / 256, 148 * 16));
-    const int kb = static_cast<int>(std::min<size_t>((krows * d + 255) / 256, 148 * 16));
+    const int sms = sm_count(dev);
+    if (sms == 0) return ATTN_ERR_CUDA;
+    const int qb = static_cast<int>(std::min<size_t>((qrows * d + 255) / 256, static_cast<size_t>(sms) * 16));
+    const int kb = static_cast<int>(std::min<size_t>((krows * d + 255) / 256, static_cast<size_t>(sms) * 16));
     if (qrows > 0) fill_empty_kernel<<<qb, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), nullptr, qrows, d);
     if (krows > 0) {
       fill_empty_kernel<<<kb, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dk), nullptr, krows, d);
@@ -590,6 +615,12 @@ uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_
 
 const char* attn_version(void) { return "exact-attn-sm103 0.1"; }
 
+attn_status attn_test_arm_stall(int kind) {
+  if (kind != 0 && kind != ATTN_TEST_STALL_PREFILL && kind != ATTN_TEST_STALL_DECODE) return ATTN_ERR_INVALID_ARG;
+  g_armed_stall.store(kind);
+  return ATTN_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -604,13 +635,13 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
 void* noalloc_scratch_ptr(int dev) {
-  static void* ptrs[kMaxDevices] = {};
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
+  static std::atomic<void*> ptrs[kMaxDevices];
+  void* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    ptrs[dev] = p;
+    ptrs[dev].store(p, std::memory_order_release);
   }
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace

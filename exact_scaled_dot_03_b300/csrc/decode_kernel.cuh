@@ -76,6 +76,10 @@ struct DecArgs {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
+  // Failure-detection test hook: when set, warp 0 of block 0 replaces its first
+  // tile wait by a wait on a barrier that nothing arrives on, with a 1 ms limit
+  // (0 in normal use).
+  int stall;
 };
 
 template <int D, int GC>
@@ -100,7 +104,9 @@ struct DecCfg {
   static constexpr int WL_OFF = WM_OFF + NW * GC * 4;             // [NW][GC] per-warp denominator
   static constexpr int BAR_OFF = WL_OFF + NW * GC * 4;            // full[STAGES]
   static constexpr int CNT_OFF = BAR_OFF + STAGES * 8;            // releases[STAGES], fills[STAGES]
+  // abort flag, last flags, plan (3 x int64 at +16), the test hook's barrier at +48
   static constexpr int MISC_OFF = CNT_OFF + 2 * STAGES * 4 + 8;
+  static_assert(MISC_OFF % 8 == 0, "mbarrier and int64 alignment");
   static constexpr int SMEM_BYTES = MISC_OFF + 64 + 1024;         // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -188,6 +194,7 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
   volatile int* last_flag = abort_flag + 1;
   long long* plan_sm = reinterpret_cast<long long*>(smem + C::MISC_OFF + 16);  // T, b_start, P_start
+  uint64_t* stall_bar = reinterpret_cast<uint64_t*>(smem + C::MISC_OFF + 48);  // test hook: never arrived on
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -200,6 +207,7 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
       releases[s] = 0;
       fills[s] = 0;
     }
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbarrier_init();
@@ -376,7 +384,13 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
     for (int jj = jbeg; jj < jend; ++jj, ++it_tile) {
       const int s = it_tile % C::STAGES;
       bool live = !*abort_flag;
-      if (live && !mbar_wait(full + s, (it_tile / C::STAGES) & 1, a.status, kSiteDecFull)) {
+      if (live && a.stall != 0 && blockIdx.x == 0 && warp == 0 && it_tile == 0) {
+        // test hook: gives up after 1 ms (nothing arrives), then takes the abort path
+        mbar_wait(stall_bar, 0, a.status, kSiteDecFull, abort_flag, kStallLimitNs);
+        *abort_flag = 1;
+        live = false;
+      }
+      if (live && !mbar_wait(full + s, (it_tile / C::STAGES) & 1, a.status, kSiteDecFull, abort_flag)) {
         *abort_flag = 1;
         live = false;
       }

@@ -50,6 +50,10 @@ struct FwdArgs {
   // at position i + causal_offset.
   const float2* rope_cs;
   int rope_pmin, rope_T;
+  // Failure-detection test hook: when set, the softmax warps of query tile 0
+  // of block (0, 0, 0) replace their first S wait by a wait on a barrier that
+  // nothing arrives on, with a 1 ms limit (0 in normal use).
+  int stall;
 };
 
 template <int D>
@@ -65,8 +69,9 @@ struct FwdCfg {
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain
-  static constexpr int NUM_BARS = 1 + 4 * STAGES + 8;  // + q_ready
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain,
+  // q_ready, stall
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 9;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + tmem base/abort words + alignment slack
   static constexpr int THREADS = 320;
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* pv_done = p_full + 2;          // [2]
   uint64_t* drain = pv_done + 2;
   uint64_t* q_ready = drain + 1;  // RoPE only: both Q tiles rotated in shared memory
+  uint64_t* stall_bar = q_ready + 1;  // test hook only: never arrived on
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(drain, 1);
     mbar_init(q_ready, 256);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -199,36 +206,39 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d_hint(sQ + t * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q, q_full, kb * 64, q_base + 128 * t,
                            b * a.Hq + h, stream_once);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;  // K and V tiles whose copies were started
       for (int js = 0; js < n_kv_max; ++js) {
         const int j = j0 + js;  // key tile
         const int s = js % C::STAGES;
         const int u = js / C::STAGES;
-        if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, a.status, kSiteKEmpty)) { *abort_flag = 1; break; }
+        if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, a.status, kSiteKEmpty, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
         mbar_arrive_expect_tx(k_full + s, C::TILE_BYTES);
         for (int kb = 0; kb < C::KBLK; ++kb)
           tma_load_3d(sK + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_k, k_full + s, kb * 64, j * 128,
                       b * a.Hkv + hkv);
-        if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, a.status, kSiteVEmpty)) {
-          *abort_flag = 1;
-          issued = js + 1;  // K of this tile is in flight, V is not
+        k_issued = js + 1;
+        if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, a.status, kSiteVEmpty, abort_flag)) {
+          *abort_flag = 1;  // K of this tile is in flight, V is not
           break;
         }
         mbar_arrive_expect_tx(v_full + s, C::TILE_BYTES);
         for (int kb = 0; kb < C::KBLK; ++kb)
           tma_load_3d(sV + s * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_v, v_full + s, kb * 64, j * 128,
                       b * a.Hkv + hkv);
-        issued = js + 1;
+        v_issued = js + 1;
         if (*abort_flag) break;
       }
       if (*abort_flag) {
-        // Let every copy still in flight land before the CTA exits.
+        // Let every copy still in flight land before the CTA exits: the last
+        // STAGES copies started into each ring (earlier ones were consumed).
         mbar_wait(q_full, 0, a.status, kSiteLoadDrain);
-        for (int js = max(0, issued - C::STAGES); js < issued; ++js) {
-          const int s = js % C::STAGES;
-          mbar_wait(k_full + s, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
-          mbar_wait(v_full + s, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
-        }
+        for (int js = max(0, k_issued - C::STAGES); js < k_issued; ++js)
+          mbar_wait(k_full + js % C::STAGES, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
+        for (int js = max(0, v_issued - C::STAGES); js < v_issued; ++js)
+          mbar_wait(v_full + js % C::STAGES, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
       }
     }
   } else if (warp == 9) {
@@ -236,19 +246,19 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && n_kv_max > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      bool ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull);
+      bool ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull, abort_flag);
       for (int js = 0; ok && js < n_kv_max; ++js) {
         const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
         const int s = js % C::STAGES;
         const uint32_t ph = (js / C::STAGES) & 1;
-        if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull))) break;
+        if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull, abort_flag))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || !uses(t, j)) continue;
           // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
           if (j > jb[t]) {
-            if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma))) break;
+            if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag))) break;
             tc_fence_after_sync();
           }
           const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
@@ -263,12 +273,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (!ok) break;
         umma_commit(k_empty + s);
-        if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull))) break;
+        if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull, abort_flag))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || !uses(t, j)) continue;
-          if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull))) break;
+          if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
           tc_fence_after_sync();
           const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
 #pragma unroll
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(320, 1)
         float2 cs[D / 2];
 #pragma unroll
         for (int i = 0; i < D / 2; ++i) cs[i] = __ldg(tab + (size_t)i * a.rope_T);
-        if (!(ok = mbar_wait(q_full, 0, a.status, kSiteQFull))) *abort_flag = 1;
+        if (!(ok = mbar_wait(q_full, 0, a.status, kSiteQFull, abort_flag))) *abort_flag = 1;
         const int rloc = wq * 32 + lane;
         uint8_t* qrow = sQ + t * C::TILE_BYTES + rloc * 128;
 #pragma unroll
@@ -339,8 +349,15 @@ __global__ void __launch_bounds__(320, 1)
       }
       mbar_arrive(q_ready);
     }
+    // test hook: the first S wait of query tile 0 in block (0, 0, 0) stalls
+    const bool stall = a.stall != 0 && t == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     for (int j = 0; ok && j < nk; ++j) {  // step j visits key tile jb[t] + j
-      if (!(ok = mbar_wait(s_full + t, j & 1, a.status, kSiteSFull))) break;
+      if (stall) {  // gives up after 1 ms (nothing arrives), then takes the abort path
+        mbar_wait(stall_bar, 0, a.status, kSiteSFull, abort_flag, kStallLimitNs);
+        ok = false;
+        break;
+      }
+      if (!(ok = mbar_wait(s_full + t, j & 1, a.status, kSiteSFull, abort_flag))) break;
       tc_fence_after_sync();
       float sv[128];
       {
@@ -405,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
       l += l0 + l1;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // Bring the accumulated u onto the new reference before P.V adds to it.
-        if (!(ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneRescale))) break;
+        if (!(ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneRescale, abort_flag))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------- epilogue
     bool have_o = false;
     if (ok && nk > 0) {
-      ok = mbar_wait(pv_done + t, (nk - 1) & 1, a.status, kSitePvDoneEpi);
+      ok = mbar_wait(pv_done + t, (nk - 1) & 1, a.status, kSitePvDoneEpi, abort_flag);
       tc_fence_after_sync();
       have_o = ok;
     }

@@ -19,6 +19,8 @@ enum : unsigned {
 // A wait longer than this is a bug (no legitimate stage of these kernels takes
 // more than a few microseconds), so the waiter records an error and bails out.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Limit of the one wait the failure-detection test hook makes stall.
+constexpr unsigned long long kStallLimitNs = 1000ull * 1000ull;  // 1 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -60,15 +62,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Slow path of a bounded wait: spin on try_wait, give up after kWaitLimitNs.
-// On give-up it ORs kStatusWaitTimeout into status[0], records the call site
-// and block in status[1..2], and returns false.
-__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, unsigned* status,
-                                                   unsigned site) {
+// Slow path of a bounded wait: spin on try_wait. Gives up after `limit_ns`:
+// ORs kStatusWaitTimeout into status[0], records the call site and block in
+// status[1..2] and returns false. If `abort_flag` is given, it also returns
+// false (recording nothing) as soon as another role of the CTA has set that
+// flag, so one give-up ends the whole CTA's pipeline within microseconds.
+// Waits that let in-flight copies or MMAs land before the CTA exits pass no
+// flag: they must run to completion.
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, unsigned* status, unsigned site,
+                                               const volatile int* abort_flag, unsigned long long limit_ns) {
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusWaitTimeout);
       atomicExch(status + 1, site);
       atomicExch(status + 2, blockIdx.x + 65536u * blockIdx.y);
@@ -78,10 +85,12 @@ __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, u
 }
 
 // Wait until the phase with the given parity has completed. Returns false on
-// timeout (see mbar_wait_slow).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status, unsigned site) {
+// timeout or, with `abort_flag`, when the CTA is aborting (see mbar_wait_slow).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status, unsigned site,
+                                          const volatile int* abort_flag = nullptr,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, status, site);
+  return mbar_wait_slow(bar, parity, status, site, abort_flag, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -164,6 +164,8 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
  * must be zero-filled before its first use; every call that completes
  * leaves it zero-filled again, so it can be reused across calls on one
  * stream (calls that overlap on the device must use separate workspaces).
+ * A call after which attn_device_status() reports ATTN_ERR_TIMEOUT can leave
+ * part-counted tickets behind: zero-fill the workspace again before reusing it.
  */
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d);
 
@@ -223,7 +225,9 @@ ATTN_API size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max
  *   page_size    a divisor of 128 that is >= 8, or a multiple of 128
  *                (others: ATTN_ERR_UNSUPPORTED).
  *   workspace    >= attn_decode_paged_workspace_size(...) bytes, zero-filled
- *                before first use, left zero-filled by every completed call.
+ *                before first use, left zero-filled by every completed call
+ *                (zero-fill it again after a call that timed out, as for
+ *                attn_decode).
  * The appended rows are the only cache memory written.
  */
 ATTN_API attn_status attn_decode_paged(const void* q, const void* k_new, const void* v_new, void* k_pages,
@@ -286,6 +290,33 @@ ATTN_API uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, i
 ATTN_API attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
                                          int Lmax, int d, float scale, void* stream);
+
+/*
+ * Test hook for failure detection. The pages have no counterpart: it exists so
+ * that the kernels' give-up path can be exercised on a GPU without a fault or
+ * a hang.
+ *
+ * Every internal wait of the kernels is bounded (1 s). When one gives up, the
+ * kernel records ATTN_ERR_TIMEOUT, the wait site and the block in the status
+ * word, every other role of that CTA stops waiting, the copies and MMAs still
+ * in flight are allowed to land, tensor memory is freed and the kernel
+ * returns; attn_device_status() then reports it.
+ *
+ * attn_test_arm_stall(kind) arms the next launch, in this process, of one
+ * kernel: in its first CTA one role waits on a barrier that nothing ever
+ * arrives on, with a 1 ms limit, instead of its first real wait:
+ *   ATTN_TEST_STALL_PREFILL  attn_fwd / _window / _rope: the softmax warps of
+ *                            query tile 0, first score tile (wait site 8)
+ *   ATTN_TEST_STALL_DECODE   attn_decode / _paged / _noalloc: warp 0, first
+ *                            K/V tile (wait site 20)
+ * The hook disarms itself at that launch; kind 0 disarms it. The outputs of
+ * the stalled launch are undefined, and a decode workspace it used must be
+ * zero-filled again before reuse (its tickets are left part-counted). Returns
+ * ATTN_ERR_INVALID_ARG for an unknown kind.
+ */
+#define ATTN_TEST_STALL_PREFILL 1
+#define ATTN_TEST_STALL_DECODE 2
+ATTN_API attn_status attn_test_arm_stall(int kind);
 
 /* Library version string, e.g. "exact-attn-sm103 0.1". */
 ATTN_API const char* attn_version(void);

@@ -197,3 +197,12 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+def test_stall_hook_host_side(lib):
+    """The failure-detection test hook accepts only its kinds (and 0, which
+    disarms it); nothing is launched here."""
+    assert lib.attn_test_arm_stall(7) == binding.ERR_INVALID_ARG
+    assert lib.attn_test_arm_stall(-1) == binding.ERR_INVALID_ARG
+    assert lib.attn_test_arm_stall(1) == binding.OK
+    assert lib.attn_test_arm_stall(0) == binding.OK   # disarmed again

@@ -169,6 +169,18 @@ def test_causal_gqa_16384_sampled():
                   compare_grad(dk[:, g:g + 1, t0:], rk, m["tk"], m["sk"], f"{w.name} dk last tile kv={g}"))
             print(w.name, "dv last tile", g,
                   compare_grad(dv[:, g:g + 1, t0:], rv, m["tv"], None, f"{w.name} dv last tile kv={g}"))
+        # key tile 0 is the heaviest: every query row of the 8 heads of its group
+        # (131 072 rows) adds to it, so it carries the most accumulated rounding;
+        # the oracle takes every row in full (row-blocked), about a minute on the host
+        g = 0
+        hs = slice(0, 8)
+        _, rk, rv, m = oracle.attention_backward(
+            f64(q[:, hs]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1]), f64(do[:, hs]), w.scale, True,
+            q_rows=np.array([], dtype=np.int64), k_rows=np.arange(128), row_block=2048, magnitudes=True)
+        print(w.name, "dk first tile", g,
+              compare_grad(dk[:, g:g + 1, :128], rk, m["tk"], m["sk"], f"{w.name} dk first tile kv={g}"))
+        print(w.name, "dv first tile", g,
+              compare_grad(dv[:, g:g + 1, :128], rv, m["tv"], None, f"{w.name} dv first tile kv={g}"))
 
     samples = [(0, 3, np.sort(rng.choice(w.Nq, 48, replace=False))),
                (0, 60, np.concatenate([np.arange(4), np.arange(w.Nq - 4, w.Nq)]))]

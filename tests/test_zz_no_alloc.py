@@ -6,8 +6,9 @@ device memory, or where an allocation could synchronise or fail). This entry
 point keeps its split-KV scratch in a static device array inside the library
 instead. Here it is called through the C ABI twice in a row, on different
 problems so the second call starts from the first call's leftover scratch,
-and each result is checked against the workspace-taking attn_decode within
-the parity tolerance the other tests use.
+and each result is checked against the fp64 oracle (the parity bar every
+other test uses) and against the workspace-taking attn_decode within the
+same tolerance.
 
 Kept in a file that pytest collects last, so a run that stops at the first
 failure has already run every other test.
@@ -17,9 +18,10 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from exact_scaled_dot_03_b300 import binding
 from exact_scaled_dot_03_b300.workloads import DECODE_GQA, Decode, decode_inputs
-from tests.parity import LSE_MAX_ABS, O_MAX_ABS, O_MEAN_ABS
+from tests.parity import LSE_MAX_ABS, O_MAX_ABS, O_MEAN_ABS, compare, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +52,10 @@ def _check_against_workspace_path(w, lens=None):
     lse = torch.empty(w.B, w.Hq, dtype=torch.float32, device="cuda")
     assert _noalloc(q, kc, vc, sl, o, lse, w.scale) == binding.OK
     torch.cuda.synchronize()
+    # against the oracle: the plain decode definition in fp64 on the same bf16 inputs
+    o64, lse64 = oracle.attention_decode(f64(q), f64(kc), f64(vc), sl.cpu().numpy(), w.scale)
+    print(w.name, compare(o, lse, o64, lse64, f"noalloc {w.name}"))
+    # and against the workspace-taking entry point
     err = (o.float() - o_ref.float()).abs()
     assert err.max().item() <= O_MAX_ABS and err.mean().item() <= O_MEAN_ABS
     finite = torch.isfinite(lse_ref)
