@@ -20,6 +20,12 @@
 // the bf16 probabilities P_t are written over the first 64 columns of S_t and
 // fed to the P.V MMA straight from TMEM.
 //
+// Head dim 64: O takes only 64 columns per tile, so P gets columns of its own
+// (P0 [384,448), P1 [448,512)) instead of sharing S's. S_t can then be
+// overwritten as soon as the softmax warps have read it: the MMA warp computes
+// S of the next key tile while the softmax works on this one (one step ahead),
+// and the softmax only waits for the previous P.V before storing the new P.
+//
 // Rescaling is lazy: the reference max m of a row only moves when the new
 // tile's max exceeds it by more than 8 (in base-2 units). l and u always share
 // the same reference, so o = u / l is unchanged in exact arithmetic; the
@@ -70,13 +76,15 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain,
-  // q_ready, stall
-  static constexpr int NUM_BARS = 1 + 4 * STAGES + 9;
+  // q_ready, stall, s_free[2]
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 11;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + tmem base/abort words + alignment slack
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
+  static constexpr bool SEP_P = (D == 64);       // P in columns of its own (see the header comment)
+  static constexpr uint32_t P_COL = 384;         // SEP_P only
 };
 
 // Wait sites (recorded in status[1] when a bounded wait gives up).
@@ -140,6 +148,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* drain = pv_done + 2;
   uint64_t* q_ready = drain + 1;  // RoPE only: both Q tiles rotated in shared memory
   uint64_t* stall_bar = q_ready + 1;  // test hook only: never arrived on
+  uint64_t* s_free = stall_bar + 1;   // [2] head dim 64: S_t read into registers
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -174,6 +183,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
       mbar_init(pv_done + t, 1);
+      mbar_init(s_free + t, 128);
     }
     mbar_init(drain, 1);
     mbar_init(q_ready, 256);
@@ -247,50 +257,107 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       bool ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull, abort_flag);
-      for (int js = 0; ok && js < n_kv_max; ++js) {
-        const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
-        const int s = js % C::STAGES;
-        const uint32_t ph = (js / C::STAGES) & 1;
-        if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull, abort_flag))) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || !uses(t, j)) continue;
-          // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
-          if (j > jb[t]) {
-            if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag))) break;
-            tc_fence_after_sync();
-          }
-          const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
-          const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-            umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
-                    smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full + t);
-        }
-        if (!ok) break;
-        umma_commit(k_empty + s);
-        if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull, abort_flag))) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || !uses(t, j)) continue;
-          if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
+      if constexpr (C::SEP_P) {
+        // S of stream position js + 1 goes out before P.V of position js.
+        int ns0 = 0, ns1 = 0;  // S steps issued for query tile 0 / 1
+        auto issue_s = [&](int js) -> bool {
+          const int j = j0 + js;
+          const int s = js % C::STAGES;
+          if (!mbar_wait(k_full + s, (js / C::STAGES) & 1, a.status, kSiteKFull, abort_flag)) return false;
           tc_fence_after_sync();
-          const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            umma_ts(tmem + C::O_COL + D * t, tmem + 128 * t + kk * 8,
-                    smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
-                    (j > jb[t] || kk > 0) ? 1u : 0u);
+          for (int t = 0; t < 2; ++t) {
+            if (!uses(t, j)) continue;
+            const int ns = t == 0 ? ns0 : ns1;
+            // S_t is overwritten: the softmax warps must have read the previous one.
+            if (ns > 0) {
+              if (!mbar_wait(s_free + t, (ns - 1) & 1, a.status, kSitePvDoneMma, abort_flag)) return false;
+              tc_fence_after_sync();
+            }
+            const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
+            const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+              umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
+                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(s_full + t);
+            if (t == 0) ++ns0; else ++ns1;
           }
-          umma_commit(pv_done + t);
+          umma_commit(k_empty + s);
+          return true;
+        };
+        ok = ok && issue_s(0);
+        for (int js = 0; ok && js < n_kv_max; ++js) {
+          if (js + 1 < n_kv_max && !(ok = issue_s(js + 1))) break;
+          const int j = j0 + js;
+          const int s = js % C::STAGES;
+          if (!(ok = mbar_wait(v_full + s, (js / C::STAGES) & 1, a.status, kSiteVFull, abort_flag))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || !uses(t, j)) continue;
+            if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
+            tc_fence_after_sync();
+            const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              umma_ts(tmem + C::O_COL + D * t, tmem + C::P_COL + 64 * t + kk * 8,
+                      smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
+                      (j > jb[t] || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(pv_done + t);
+          }
+          if (!ok) break;
+          umma_commit(v_empty + s);
         }
-        if (!ok) break;
-        umma_commit(v_empty + s);
+      } else {
+        for (int js = 0; ok && js < n_kv_max; ++js) {
+          const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
+          const int s = js % C::STAGES;
+          const uint32_t ph = (js / C::STAGES) & 1;
+          if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull, abort_flag))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || !uses(t, j)) continue;
+            // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
+            if (j > jb[t]) {
+              if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag))) break;
+              tc_fence_after_sync();
+            }
+            const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
+            const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+              umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
+                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(s_full + t);
+          }
+          if (!ok) break;
+          umma_commit(k_empty + s);
+          if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull, abort_flag))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || !uses(t, j)) continue;
+            if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
+            tc_fence_after_sync();
+            const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              umma_ts(tmem + C::O_COL + D * t, tmem + 128 * t + kk * 8,
+                      smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
+                      (j > jb[t] || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(pv_done + t);
+          }
+          if (!ok) break;
+          umma_commit(v_empty + s);
+        }
       }
       if (!ok) *abort_flag = 1;
       // Every MMA issued above has finished before TMEM is released.
@@ -305,6 +372,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * t;
     const uint32_t tO = tmem + lane_off + C::O_COL + D * t;
+    const uint32_t tP = C::SEP_P ? tmem + lane_off + C::P_COL + 64 * t : tS;  // where P is stored
     const int nk = t == 0 ? n_kv[0] : n_kv[1];   // selects, not a dynamic index (keeps them in registers)
     const int jb_t = t == 0 ? jb[0] : jb[1];
     const float sl2 = a.scale_log2;
@@ -372,6 +440,10 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(sr[c][i]);
         }
       }
+      if constexpr (C::SEP_P) {  // S_t is in registers: the MMA warp may compute the next one into it
+        tc_fence_before_sync();
+        mbar_arrive(s_free + t);
+      }
       const int key0 = (jb_t + j) * 128;
       if (key0 + 127 > hi_first || (WIN && key0 < lo_last)) {  // tile-uniform: an edge crosses the tile
         const int rel_lo = vis_lo - key0, rel_hi = vis_hi - key0;
@@ -417,8 +489,18 @@ __global__ void __launch_bounds__(320, 1)
           add2(l0, l1, p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tS + 32 * half, pk);
+        if (C::SEP_P && half == 0 && j > 0) {
+          // P_t's columns are free once the previous P.V has read them.
+          ok = mbar_wait(pv_done + t, (j - 1) & 1, a.status, kSitePvDoneRescale, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform: the TMEM stores below are warp-collective
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        tmem_st32(tP + 32 * half, pk);
       }
+      if (!ok) break;
       l += l0 + l1;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // Bring the accumulated u onto the new reference before P.V adds to it.
