@@ -24,6 +24,8 @@ _vp, _i, _f, _sz, _i64, _u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, c
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "attn_fwd_host_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "attn_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "attn_fwd_rope_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_fwd_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _vp, _sz, _vp]),
     "attn_bwd_workspace_size": (_sz, [_i, _i, _i]),
@@ -121,6 +123,59 @@ def fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, w
                                  lse.data_ptr() if lse is not None else None,
                                  B, Hq, Hkv, Nq, Nk, d, s, int(bool(causal)), int(window), _stream_handle(stream))
     _check(code, "attn_fwd_window")
+    return o, lse
+
+
+def _need_host(t: torch.Tensor, name: str, dtype=torch.bfloat16, dims=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+
+
+def fwd_host_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(lib().attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d))
+
+
+def fwd_host(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+             workspace=None, stream=None, device=None):
+    """Prefill on host tensors: returns (o, lse) in host memory; see ``attn_fwd_host``
+    in include/attn.h. Pinned tensors (``pin_memory()``) let the copies overlap
+    the kernels. The results are complete once ``stream`` has passed the call
+    (``stream.synchronize()``); the call itself returns as soon as the work is queued.
+
+    q: [B, Hq, Nq, d], k/v: [B, Hkv, Nk, d], bf16 host tensors; workspace: a uint8
+    CUDA tensor of at least ``fwd_host_workspace_size`` bytes (allocated here if None).
+    """
+    _need_host(q, "q", dims=4)
+    _need_host(k, "k", dims=4)
+    _need_host(v, "v", dims=4)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if k.shape != v.shape or Bk != B or dk != d:
+        raise ValueError("q/k/v shapes disagree")
+    pin = q.is_pinned()
+    o = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if out is None else out
+    _need_host(o, "out", dims=4)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=pin)
+    if lse is not None:
+        _need_host(lse, "lse", dtype=torch.float32, dims=3)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    need = fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", dtype=torch.uint8)
+    s = default_scale(d) if scale is None else float(scale)
+    with torch.cuda.device(workspace.device):
+        code = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Nq, Nk, d, s,
+                                   int(bool(causal)), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(code, "attn_fwd_host")
     return o, lse
 
 

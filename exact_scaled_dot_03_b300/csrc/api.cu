@@ -372,6 +372,170 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
 }
 
 namespace {
+// ---------------------------------------------------------------- host-buffer prefill
+// Staging in the caller's workspace (every piece 256-byte aligned):
+//   kHostKvSlots  x (K, V of one (batch, KV head) group)
+//   ATTN_FWD_HOST_SLOTS x (Q, O, LSE of one chunk: up to all G query heads of a group)
+constexpr int kHostKvSlots = 2;
+struct HostPlan {
+  size_t q_bytes, kv_bytes, lse_bytes;  // per query head (q, o, lse) and per group (k, v)
+  size_t kv_slot, q_slot, o_off, lse_off, q_base, total;
+};
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool plan_host(int B, int Hq, int Hkv, int Nq, int Nk, int d, HostPlan* p) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return false;
+  const size_t G = static_cast<size_t>(Hq / Hkv);
+  p->q_bytes = static_cast<size_t>(Nq) * d * 2;
+  p->kv_bytes = static_cast<size_t>(Nk) * d * 2;
+  p->lse_bytes = static_cast<size_t>(Nq) * 4;
+  p->kv_slot = 2 * align256(p->kv_bytes);
+  p->o_off = align256(G * p->q_bytes);
+  p->lse_off = p->o_off + align256(G * p->q_bytes);
+  p->q_slot = p->lse_off + align256(G * p->lse_bytes);
+  p->q_base = kHostKvSlots * p->kv_slot;
+  p->total = p->q_base + ATTN_FWD_HOST_SLOTS * p->q_slot;
+  return true;
+}
+
+// Query heads per chunk: the largest divisor of the group size G whose chunk
+// still fills about two CTAs per SM (a chunk of heads * ceil(Nq/256) CTAs).
+// Smaller chunks shorten the start and end of the pipeline, where only one
+// copy direction is busy; G heads (one chunk per group) when even a single
+// head has that many CTAs.
+int host_heads_per_chunk(int G, int Nq, int sms) {
+  const long long pairs = (Nq + 255) / 256;
+  const long long target = 2LL * sms;
+  int best = 1;
+  for (int h = 1; h <= G; ++h)
+    if (G % h == 0 && h * pairs <= target) best = h;
+  return best;
+}
+
+// The copy streams and events of one device, created on its first call.
+struct HostPipe {
+  std::mutex mu;  // calls on one device queue their work one at a time
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t entry = nullptr, last = nullptr;
+  cudaEvent_t in_done[ATTN_FWD_HOST_SLOTS] = {}, comp_done[ATTN_FWD_HOST_SLOTS] = {},
+              out_done[ATTN_FWD_HOST_SLOTS] = {}, kv_free[kHostKvSlots] = {};
+};
+HostPipe& host_pipe(int dev) {
+  static HostPipe pipes[kMaxDevices];
+  return pipes[dev];
+}
+bool host_pipe_init(HostPipe& p) {
+  if (p.ready) return true;
+  auto ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+  if (cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking) != cudaSuccess || !ev(&p.entry) || !ev(&p.last))
+    return false;
+  for (int i = 0; i < ATTN_FWD_HOST_SLOTS; ++i)
+    if (!ev(&p.in_done[i]) || !ev(&p.comp_done[i]) || !ev(&p.out_done[i])) return false;
+  for (int i = 0; i < kHostKvSlots; ++i)
+    if (!ev(&p.kv_free[i])) return false;
+  p.ready = true;
+  return true;
+}
+}  // namespace
+
+size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  HostPlan p;
+  return plan_host(B, Hq, Hkv, Nq, Nk, d, &p) ? p.total : 0;
+}
+
+attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  // q, o may be NULL only when there are no queries, k, v only when there are no keys.
+  if ((Nq > 0 && (q == nullptr || o == nullptr)) || (Nk > 0 && (k == nullptr || v == nullptr)))
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || (Nq + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  HostPlan plan;
+  if (!plan_host(B, Hq, Hkv, Nq, Nk, d, &plan)) return ATTN_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < plan.total) return ATTN_ERR_INVALID_ARG;
+  if (Nq == 0) return ATTN_OK;
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  const int sms = sm_count(dev);
+  if (sms == 0) return ATTN_ERR_CUDA;
+  HostPipe& P = host_pipe(dev);
+  std::lock_guard<std::mutex> lock(P.mu);
+  if (!host_pipe_init(P)) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = Hq / Hkv;
+  const int hc = host_heads_per_chunk(G, Nq, sms);  // query heads per chunk
+  const int per_group = G / hc;
+  const int groups = B * Hkv;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* qh = static_cast<const uint8_t*>(q);
+  const uint8_t* kh = static_cast<const uint8_t*>(k);
+  const uint8_t* vh = static_cast<const uint8_t*>(v);
+  uint8_t* oh = static_cast<uint8_t*>(o);
+  uint8_t* lh = reinterpret_cast<uint8_t*>(lse);
+  const size_t cq = hc * plan.q_bytes, cl = hc * plan.lse_bytes;  // bytes of one chunk's Q (= O) and LSE
+  bool ok = true;
+  attn_status st = ATTN_OK;
+  auto chk = [&](cudaError_t e) { ok = ok && (e == cudaSuccess); };
+  // Nothing starts before the work queued on `stream` up to this call.
+  chk(cudaEventRecord(P.entry, s));
+  chk(cudaStreamWaitEvent(P.s_in, P.entry, 0));
+  chk(cudaStreamWaitEvent(P.s_out, P.entry, 0));
+  int c = 0;  // chunk index over the whole call
+  for (int grp = 0; grp < groups && ok && st == ATTN_OK; ++grp) {
+    // group grp = (batch b, KV head g): its query heads g*G .. g*G+G-1 of batch b are
+    // contiguous in Q, O and LSE, so chunk c covers bytes [c*cq, (c+1)*cq) of Q and O.
+    const int ks = grp % kHostKvSlots;
+    uint8_t* kd = ws + ks * plan.kv_slot;
+    uint8_t* vd = kd + align256(plan.kv_bytes);
+    if (Nk > 0) {
+      // the K/V slot is free once every chunk of group grp - kHostKvSlots has run
+      if (grp >= kHostKvSlots) chk(cudaStreamWaitEvent(P.s_in, P.kv_free[ks], 0));
+      const size_t ko = static_cast<size_t>(grp) * plan.kv_bytes;
+      chk(cudaMemcpyAsync(kd, kh + ko, plan.kv_bytes, cudaMemcpyHostToDevice, P.s_in));
+      chk(cudaMemcpyAsync(vd, vh + ko, plan.kv_bytes, cudaMemcpyHostToDevice, P.s_in));
+    }
+    for (int j = 0; j < per_group && ok; ++j, ++c) {
+      const int slot = c % ATTN_FWD_HOST_SLOTS;
+      uint8_t* base = ws + plan.q_base + slot * plan.q_slot;
+      // copy in: the slot's Q is free once the prefill of chunk c - SLOTS is done
+      // (the K/V copies above precede it on the same stream)
+      if (c >= ATTN_FWD_HOST_SLOTS) chk(cudaStreamWaitEvent(P.s_in, P.comp_done[slot], 0));
+      chk(cudaMemcpyAsync(base, qh + c * cq, cq, cudaMemcpyHostToDevice, P.s_in));
+      chk(cudaEventRecord(P.in_done[slot], P.s_in));
+      // prefill on `stream`: the slot's O, LSE are free once the copy out of chunk c - SLOTS is done
+      chk(cudaStreamWaitEvent(s, P.in_done[slot], 0));
+      if (c >= ATTN_FWD_HOST_SLOTS) chk(cudaStreamWaitEvent(s, P.out_done[slot], 0));
+      if (!ok) break;
+      st = attn_fwd(base, Nk > 0 ? kd : nullptr, Nk > 0 ? vd : nullptr, base + plan.o_off,
+                    lse != nullptr ? reinterpret_cast<float*>(base + plan.lse_off) : nullptr, 1, hc, 1, Nq, Nk, d,
+                    scale, causal, s);
+      if (st != ATTN_OK) break;
+      chk(cudaEventRecord(P.comp_done[slot], s));
+      if (j == per_group - 1) chk(cudaEventRecord(P.kv_free[ks], s));
+      // copy out
+      chk(cudaStreamWaitEvent(P.s_out, P.comp_done[slot], 0));
+      chk(cudaMemcpyAsync(oh + c * cq, base + plan.o_off, cq, cudaMemcpyDeviceToHost, P.s_out));
+      if (lse != nullptr)
+        chk(cudaMemcpyAsync(lh + c * cl, base + plan.lse_off, cl, cudaMemcpyDeviceToHost, P.s_out));
+      chk(cudaEventRecord(P.out_done[slot], P.s_out));
+    }
+  }
+  // `stream` passes this call once every copy out has landed (and the copy-in
+  // stream has finished with the workspace).
+  chk(cudaEventRecord(P.last, P.s_out));
+  chk(cudaStreamWaitEvent(s, P.last, 0));
+  chk(cudaEventRecord(P.last, P.s_in));
+  chk(cudaStreamWaitEvent(s, P.last, 0));
+  if (st != ATTN_OK) return st;
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+namespace {
 // RoPE workspace: the rotated K ([B, Hkv, Nk, d] bf16), then the (cos, sin)
 // table of positions min(0, Nk - Nq) .. Nk - 1, position-major and pair-major.
 struct RopePlan {

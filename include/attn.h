@@ -98,6 +98,39 @@ ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v
                                      void* stream);
 
 /*
+ * attn_fwd on tensors that live in host memory. The same operation and
+ * arguments as attn_fwd ([MG-A] §2.2-§2.4, §4.1), except that q, k, v, o and
+ * lse are HOST pointers (page-locked memory lets the copies overlap; pageable
+ * memory works but the copies then serialise).
+ *
+ * Work moves in chunks: the K and V of one (batch, KV head) group go to the
+ * device once, then its query heads in chunks of a few heads each (as many as
+ * fill about two CTAs per SM): a chunk's Q goes in, the prefill runs on it,
+ * its O and LSE come back. Chunks are pipelined through ATTN_FWD_HOST_SLOTS
+ * staging slots (and K, V through two) of the caller's device workspace, so
+ * the copy in of one chunk, the prefill of the one before and the copy out of
+ * the one before that run at the same time (two copy streams of the library
+ * beside `stream`, which runs the prefill kernels). The result is bit for bit
+ * that of attn_fwd. The call returns once everything is queued; when `stream`
+ * has reached the point of the call, o and lse are complete in host memory.
+ *
+ *   workspace / workspace_bytes: device memory of at least
+ *       attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d) bytes, 256-byte
+ *       aligned, not touched by anything else until `stream` passes the call.
+ *   The first call on a device creates the two copy streams and the events
+ *   it synchronises with (kept until the process exits). Calls on one device
+ *   are serialised on the host while they queue their work.
+ *   q and o may be NULL when Nq == 0, k and v when Nk == 0.
+ *   Returns the errors of attn_fwd, plus ATTN_ERR_INVALID_ARG for a missing
+ *   or too small workspace.
+ */
+#define ATTN_FWD_HOST_SLOTS 3
+ATTN_API size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+ATTN_API attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                   int Hkv, int Nq, int Nk, int d, float scale, int causal, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * Workspace bytes attn_fwd_rope needs: the rotated K ([B, Hkv, Nk, d] bf16)
  * and two layouts (position-major, pair-major) of a (cos, sin) table of
  * max(Nk, Nq) positions x d/2 pairs (fp32).
