@@ -15,7 +15,12 @@
 //   warps 0-3 : softmax for query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7 : softmax for query tile 1
 //   warp  8   : TMA producer (Q once, then the K/V ring)
-//   warp  9   : TMEM allocator + tcgen05.mma issuer
+//   warp  9   : TMEM allocator + issuer of the S = Q K^T MMAs
+//   warp 10   : issuer of the O += P V MMAs
+// Two issuers: every barrier wait of an issuing thread is a round trip of a
+// few hundred cycles and every tcgen05.mma costs the thread tens of cycles,
+// so one thread issuing everything cannot keep the tensor core fed; split,
+// each waits only for its own inputs and their waits overlap.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
 // the bf16 probabilities P_t are written over the first 64 columns of S_t and
 // fed to the P.V MMA straight from TMEM.
@@ -80,7 +85,7 @@ struct FwdCfg {
   static constexpr int NUM_BARS = 1 + 4 * STAGES + 11;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + tmem base/abort words + alignment slack
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
   static constexpr bool SEP_P = (D == 64);       // P in columns of its own (see the header comment)
@@ -127,7 +132,7 @@ __device__ __forceinline__ void fwd_kv_tiles(const FwdArgs& a, int r0, int& jb, 
 // WIN: a local window is in force (the windowless instance keeps every range
 // offset a compile-time zero).
 template <int D, bool WIN>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(pv_done + t, 1);
       mbar_init(s_free + t, 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // one commit from each MMA issuer
     mbar_init(q_ready, 256);
     mbar_init(stall_bar, 1);
     *abort_flag = 0;
@@ -251,46 +256,54 @@ __global__ void __launch_bounds__(320, 1)
           mbar_wait(v_full + js % C::STAGES, (js / C::STAGES) & 1, a.status, kSiteLoadDrain);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each descriptor is a precomputed low word plus a compile-time offset
+    // (see sw128_desc_lo), which keeps the issuing thread's own instructions few.
     if (lane == 0 && n_kv_max > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      bool ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull, abort_flag);
-      if constexpr (C::SEP_P) {
-        // S of stream position js + 1 goes out before P.V of position js.
-        int ns0 = 0, ns1 = 0;  // S steps issued for query tile 0 / 1
-        auto issue_s = [&](int js) -> bool {
-          const int j = j0 + js;
+      constexpr uint32_t kHi = sw128_desc_hi(1024);            // 8-row atoms 1024 bytes apart
+      constexpr uint32_t kTileW = C::TILE_BYTES >> 4;          // one tile, in descriptor address units
+      bool ok = true;
+      if (warp == 9) {
+        // S_t = Q_t K^T for every key tile, over head-dim steps of 16
+        const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ), 16);  // K-major Q and K
+        const uint32_t k_lo = sw128_desc_lo(smem_u32(sK), 16);
+        ok = mbar_wait(a.rope_cs != nullptr ? q_ready : q_full, 0, a.status, kSiteQFull, abort_flag);
+        for (int js = 0; ok && js < n_kv_max; ++js) {
+          const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
           const int s = js % C::STAGES;
-          if (!mbar_wait(k_full + s, (js / C::STAGES) & 1, a.status, kSiteKFull, abort_flag)) return false;
+          if (!(ok = mbar_wait(k_full + s, (js / C::STAGES) & 1, a.status, kSiteKFull, abort_flag))) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (!uses(t, j)) continue;
-            const int ns = t == 0 ? ns0 : ns1;
-            // S_t is overwritten: the softmax warps must have read the previous one.
-            if (ns > 0) {
-              if (!mbar_wait(s_free + t, (ns - 1) & 1, a.status, kSitePvDoneMma, abort_flag)) return false;
+            if (!ok || !uses(t, j)) continue;
+            if (j > jb[t]) {
+              // S_t is overwritten: with P aliased on S the previous P.V must be done,
+              // with P in columns of its own the softmax must have read the previous S.
+              if constexpr (C::SEP_P)
+                ok = mbar_wait(s_free + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag);
+              else
+                ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag);
+              if (!ok) break;
               tc_fence_after_sync();
             }
-            const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
-            const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+            const uint32_t a0 = q_lo + t * kTileW, b0 = k_lo + s * kTileW;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-              umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+              const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+              umma_ss_w(tmem + 128 * t, a0 + off, kHi, b0 + off, kHi, idesc_qk, kk > 0 ? 1u : 0u);
             }
             umma_commit(s_full + t);
-            if (t == 0) ++ns0; else ++ns1;
           }
+          if (!ok) break;
           umma_commit(k_empty + s);
-          return true;
-        };
-        ok = ok && issue_s(0);
+        }
+      } else {
+        // O_t += P_t V for every key tile, over key steps of 16; P_t is read from TMEM
+        const uint32_t v_lo = sw128_desc_lo(smem_u32(sV), C::BLOCK_BYTES);  // MN-major V
         for (int js = 0; ok && js < n_kv_max; ++js) {
-          if (js + 1 < n_kv_max && !(ok = issue_s(js + 1))) break;
           const int j = j0 + js;
           const int s = js % C::STAGES;
           if (!(ok = mbar_wait(v_full + s, (js / C::STAGES) & 1, a.status, kSiteVFull, abort_flag))) break;
@@ -300,59 +313,12 @@ __global__ void __launch_bounds__(320, 1)
             if (!ok || !uses(t, j)) continue;
             if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
             tc_fence_after_sync();
-            const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
+            const uint32_t p_col = C::SEP_P ? C::P_COL + 64 * t : 128 * t;
+            const uint32_t b0 = v_lo + s * kTileW;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              umma_ts(tmem + C::O_COL + D * t, tmem + C::P_COL + 64 * t + kk * 8,
-                      smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
-                      (j > jb[t] || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(pv_done + t);
-          }
-          if (!ok) break;
-          umma_commit(v_empty + s);
-        }
-      } else {
-        for (int js = 0; ok && js < n_kv_max; ++js) {
-          const int j = j0 + js;  // key tile; query tile t is at its step j - jb[t]
-          const int s = js % C::STAGES;
-          const uint32_t ph = (js / C::STAGES) & 1;
-          if (!(ok = mbar_wait(k_full + s, ph, a.status, kSiteKFull, abort_flag))) break;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok || !uses(t, j)) continue;
-            // S_t is overwritten: the previous P_t (aliased on S_t) must be consumed.
-            if (j > jb[t]) {
-              if (!(ok = mbar_wait(pv_done + t, (j - jb[t] - 1) & 1, a.status, kSitePvDoneMma, abort_flag))) break;
-              tc_fence_after_sync();
-            }
-            const uint32_t q_addr = smem_u32(sQ + t * C::TILE_BYTES);
-            const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-              umma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(s_full + t);
-          }
-          if (!ok) break;
-          umma_commit(k_empty + s);
-          if (!(ok = mbar_wait(v_full + s, ph, a.status, kSiteVFull, abort_flag))) break;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok || !uses(t, j)) continue;
-            if (!(ok = mbar_wait(p_full + t, (j - jb[t]) & 1, a.status, kSitePFull, abort_flag))) break;
-            tc_fence_after_sync();
-            const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              umma_ts(tmem + C::O_COL + D * t, tmem + 128 * t + kk * 8,
-                      smem_desc_sw128(v_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
-                      (j > jb[t] || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts_w(tmem + C::O_COL + D * t, tmem + p_col + kk * 8, b0 + kk * (16 * 128 >> 4), kHi, idesc_pv,
+                        (j > jb[t] || kk > 0) ? 1u : 0u);
             umma_commit(pv_done + t);
           }
           if (!ok) break;
@@ -360,7 +326,8 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (!ok) *abort_flag = 1;
-      // Every MMA issued above has finished before TMEM is released.
+      // Every MMA either issuer started has finished before TMEM is released
+      // (the barrier completes once both have committed).
       umma_commit(drain);
       mbar_wait(drain, 0, a.status, kSiteDrain);
     }
