@@ -23,7 +23,11 @@
 //                        dQ accumulates in TMEM.
 // Both main kernels: warps 0-7 elementwise (two warpgroups, each owning half
 // g of the 128 columns of a score tile; thread = TMEM lane = row), warp 8 TMA
-// producer, warp 9 TMEM allocator + tcgen05.mma issuer. The elementwise work
+// producer, warp 9 TMEM allocator + issuer of the score-shaped MMAs (S^T and
+// dP^T, or S and dP), warp 10 issuer of the accumulating MMAs (dV and dK, or
+// dQ): a barrier wait costs an issuing thread a round trip of a few hundred
+// cycles, so two issuers whose waits overlap keep the tensor core fed where
+// one could not. The elementwise work
 // of a step runs in two phases, P = exp2(S - lse) (the exponentials) as soon
 // as S is in TMEM and dS = P (dP - Dl) once dP is, so each phase overlaps a
 // different MMA group (all MMAs are M = N = 128). In the dK/dV kernel, where
@@ -70,7 +74,7 @@ struct BwdCfg {
   static constexpr int TILE_BYTES = KBLK * BLOCK_BYTES;
   static constexpr int STAGES = (D == 128) ? 2 : 4;
   static constexpr int SEED_BYTES = 128 * 16 * 2;    // one 128 x 16 bf16 seed operand
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
 
   // dK/dV kernel: K, V once; Q, dO and (lse2, Dl) per stage.
@@ -95,8 +99,9 @@ struct BwdCfg {
   static constexpr int Q_K_OFF = 2 * TILE_BYTES;
   static constexpr int Q_V_OFF = Q_K_OFF + STAGES * TILE_BYTES;
   static constexpr int Q_BAR_OFF = Q_V_OFF + STAGES * TILE_BYTES;
-  // q_full, full[S], empty[S], s_full[2] (one per S buffer), dp_full, ds_full[2], dq_done, acc_done, drain
-  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 9;
+  // q_full, full[S], empty[S], s_full[2] (one per S buffer), dp_full, ds_full[2], dq_done, acc_done, drain,
+  // s_free[2] (one per S buffer)
+  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 11;
   static constexpr int Q_MISC_OFF = Q_BAR_OFF + Q_NUM_BARS * 8;
   static constexpr int Q_SMEM_BYTES = Q_MISC_OFF + 16 + 1024;
   // TMEM columns: S buffer 0, dP (dS written back over it), dQ, S buffer 1.
@@ -217,7 +222,7 @@ __device__ __forceinline__ void bwd_store32(uint32_t taddr, bool have, float mul
 
 // ============================================================== dK, dV
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const BwdArgs a) {
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(empty + s, 2);  // released by both MMA issuers
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -332,75 +337,87 @@ __global__ void __launch_bounds__(320, 1)
           mbar_wait(full + n % C::STAGES, (n / C::STAGES) & 1, a.status, kSiteBwdLoadDrain);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 9: S^T and dP^T; warp 10: dV and dK. The stage's Q and dO reach
+    // warp 10's MMAs through warp 9's wait on the stage (whose S^T commit the
+    // elementwise warps wait for before they release P^T).
     if (lane == 0 && n_steps > 0) {
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      bool ok = mbar_wait(kv_full, 0, a.status, kSiteBwdKvFull);
-      for (int n = 0; ok && n < n_steps; ++n) {
-        const int s = n % C::STAGES;
-        if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull))) break;
-        const uint32_t q_addr = smem_u32(sQ + s * C::TILE_BYTES);
-        const uint32_t do_addr = smem_u32(sDO + s * C::TILE_BYTES);
-        const uint32_t seed_addr = smem_u32(sSEED + s * 2 * C::SEED_BYTES);
+      constexpr uint32_t kHi = sw128_desc_hi(1024);
+      constexpr uint32_t kTileW = C::TILE_BYTES >> 4;
+      const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ), 16), do_lo = sw128_desc_lo(smem_u32(sDO), 16);
+      bool ok = true;
+      if (warp == 9) {
+        const uint32_t k_lo = sw128_desc_lo(smem_u32(sK), 16), v_lo = sw128_desc_lo(smem_u32(sV), 16);
         const uint64_t ones_desc = smem_desc_noswizzle(smem_u32(sONES), 128, 256);
-        // S^T = -lse/scale (seed MMA) + K Q^T; it overwrites P^T of the
-        // previous step (read by its dV MMAs).
-        if (n > 0 && !(ok = mbar_wait(dv_done, (n - 1) & 1, a.status, kSiteBwdDvDone))) break;
-        tc_fence_after_sync();
-        umma_ss(tmem + C::T_ST, ones_desc, smem_desc_noswizzle(seed_addr, 128, 256), idesc_ss, 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          umma_ss(tmem + C::T_ST, smem_desc_sw128(k_addr + off, 16, 1024), smem_desc_sw128(q_addr + off, 16, 1024),
-                  idesc_ss, 1u);
-        }
-        umma_commit(s_full);
-        // dP^T = -Dl (seed MMA) + V dO^T; it overwrites dS^T of the previous
-        // step (read by its dK MMAs).
-        if (n > 0 && !(ok = mbar_wait(dk_done, (n - 1) & 1, a.status, kSiteBwdDkDone))) break;
-        tc_fence_after_sync();
-        umma_ss(tmem + C::T_DPT, ones_desc, smem_desc_noswizzle(seed_addr + C::SEED_BYTES, 128, 256), idesc_ss, 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          umma_ss(tmem + C::T_DPT, smem_desc_sw128(v_addr + off, 16, 1024),
-                  smem_desc_sw128(do_addr + off, 16, 1024), idesc_ss, 1u);
-        }
-        umma_commit(dp_full);
-        // dV += P^T dO, one half of the queries as soon as its warpgroup wrote P^T.
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull))) break;
+        ok = mbar_wait(kv_full, 0, a.status, kSiteBwdKvFull, abort_flag);
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int s = n % C::STAGES;
+          if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull, abort_flag))) break;
+          const uint32_t seed_addr = smem_u32(sSEED + s * 2 * C::SEED_BYTES);
+          // S^T = -lse/scale (seed MMA) + K Q^T; it overwrites P^T of the
+          // previous step (read by its dV MMAs).
+          if (n > 0 && !(ok = mbar_wait(dv_done, (n - 1) & 1, a.status, kSiteBwdDvDone, abort_flag))) break;
           tc_fence_after_sync();
+          umma_ss(tmem + C::T_ST, ones_desc, smem_desc_noswizzle(seed_addr, 128, 256), idesc_ss, 0u);
 #pragma unroll
-          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
-            umma_ts(tmem + C::T_DV, tmem + C::T_ST + bwd_packed_col(kk),
-                    smem_desc_sw128(do_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
-                    (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        umma_commit(dv_done);
-        // dK += dS^T Q, likewise per half.
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull))) break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+            umma_ss_w(tmem + C::T_ST, k_lo + off, kHi, q_lo + s * kTileW + off, kHi, idesc_ss, 1u);
+          }
+          umma_commit(s_full);
+          // dP^T = -Dl (seed MMA) + V dO^T; it overwrites dS^T of the previous
+          // step (read by its dK MMAs).
+          if (n > 0 && !(ok = mbar_wait(dk_done, (n - 1) & 1, a.status, kSiteBwdDkDone, abort_flag))) break;
           tc_fence_after_sync();
+          umma_ss(tmem + C::T_DPT, ones_desc, smem_desc_noswizzle(seed_addr + C::SEED_BYTES, 128, 256), idesc_ss, 0u);
 #pragma unroll
-          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
-            umma_ts(tmem + C::T_DK, tmem + C::T_DPT + bwd_packed_col(kk),
-                    smem_desc_sw128(q_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
-                    (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+            umma_ss_w(tmem + C::T_DPT, v_lo + off, kHi, do_lo + s * kTileW + off, kHi, idesc_ss, 1u);
+          }
+          umma_commit(dp_full);
+          umma_commit(empty + s);  // this issuer's reads of the stage
         }
-        if (!ok) break;
-        umma_commit(dk_done);
-        umma_commit(empty + s);
+      } else {
+        // B operands (dO for dV, Q for dK) are MN-major here: K steps of 16 rows
+        const uint32_t qm_lo = sw128_desc_lo(smem_u32(sQ), C::BLOCK_BYTES);
+        const uint32_t dom_lo = sw128_desc_lo(smem_u32(sDO), C::BLOCK_BYTES);
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int s = n % C::STAGES;
+          // dV += P^T dO, one half of the queries as soon as its warpgroup wrote P^T.
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!(ok = mbar_wait(p_full + g, n & 1, a.status, kSiteBwdPFull, abort_flag))) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+              umma_ts_w(tmem + C::T_DV, tmem + C::T_ST + bwd_packed_col(kk), dom_lo + s * kTileW + kk * (16 * 128 >> 4),
+                        kHi, idesc_ts, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          umma_commit(dv_done);
+          // dK += dS^T Q, likewise per half.
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull, abort_flag))) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+              umma_ts_w(tmem + C::T_DK, tmem + C::T_DPT + bwd_packed_col(kk), qm_lo + s * kTileW + kk * (16 * 128 >> 4),
+                        kHi, idesc_ts, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          umma_commit(dk_done);
+          umma_commit(empty + s);  // this issuer's reads of the stage
+        }
+        umma_commit(acc_done);
       }
       if (!ok) *abort_flag = 1;
-      umma_commit(acc_done);
-      // Every MMA issued above has finished before TMEM is released.
+      // Every MMA either issuer started has finished before TMEM is released
+      // (the barrier completes once both have committed).
       umma_commit(drain);
       mbar_wait(drain, 0, a.status, kSiteBwdDrain);
     }
@@ -499,7 +516,7 @@ __global__ void __launch_bounds__(320, 1)
 
 // ============================================================== dQ
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdArgs a) {
@@ -520,6 +537,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* dq_done = ds_full + 2;
   uint64_t* acc_done = dq_done + 1;
   uint64_t* drain = acc_done + 1;
+  uint64_t* s_free = drain + 1;          // [2] the elementwise warps read S buffer b into registers
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::Q_MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::Q_MISC_OFF + 4);
 
@@ -540,7 +558,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(empty + s, 2);  // released by both MMA issuers
     }
     mbar_init(s_full, 1);
     mbar_init(s_full + 1, 1);
@@ -549,7 +567,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(ds_full + 1, 128);
     mbar_init(dq_done, 1);
     mbar_init(acc_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // one commit from each MMA issuer
+    mbar_init(s_free, 256);
+    mbar_init(s_free + 1, 256);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -593,67 +613,69 @@ __global__ void __launch_bounds__(320, 1)
           mbar_wait(full + n % C::STAGES, (n / C::STAGES) & 1, a.status, kSiteBwdLoadDrain);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 9: S(n) and dP(n); warp 10: dQ. The stage's K reaches warp 10's
+    // MMAs through warp 9's wait on the stage (whose S commit the elementwise
+    // warps wait for before they release dS).
     if (lane == 0 && n_kt > 0) {
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-      // S(n) = Q K_n^T into S buffer n & 1; its barrier is s_full[n & 1].
-      auto issue_s = [&](int n) {
-        const uint32_t k_addr = smem_u32(sK + (n % C::STAGES) * C::TILE_BYTES);
-        const uint32_t dst = tmem + ((n & 1) ? C::T_S1 : C::T_S0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          umma_ss(dst, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024), idesc_ss,
-                  kk > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full + (n & 1));
-      };
-      bool ok = mbar_wait(q_full, 0, a.status, kSiteBwdQFull) && mbar_wait(full, 0, a.status, kSiteBwdFull);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0);
-      }
-      for (int n = 0; ok && n < n_kt; ++n) {
-        const int s = n % C::STAGES;
-        // dP(n) overwrites dS(n-1) (read by dQ(n-1)).
-        if (n > 0 && !(ok = mbar_wait(dq_done, (n - 1) & 1, a.status, kSiteBwdDqDone))) break;
-        tc_fence_after_sync();
-        const uint32_t v_addr = smem_u32(sV + s * C::TILE_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          umma_ss(tmem + C::T_DP, smem_desc_sw128(do_addr + off, 16, 1024), smem_desc_sw128(v_addr + off, 16, 1024),
-                  idesc_ss, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(dp_full);
-        // S(n+1) into the other buffer, whose S(n-1) the elementwise warps read
-        // before signalling dS(n-1), which was waited for before dQ(n-1).
-        if (n + 1 < n_kt) {
-          if (!(ok = mbar_wait(full + (n + 1) % C::STAGES, ((n + 1) / C::STAGES) & 1, a.status, kSiteBwdFull)))
+      constexpr uint32_t kHi = sw128_desc_hi(1024);
+      constexpr uint32_t kTileW = C::TILE_BYTES >> 4;
+      bool ok = true;
+      if (warp == 9) {
+        const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ), 16), do_lo = sw128_desc_lo(smem_u32(sDO), 16);
+        const uint32_t k_lo = sw128_desc_lo(smem_u32(sK), 16), v_lo = sw128_desc_lo(smem_u32(sV), 16);
+        ok = mbar_wait(q_full, 0, a.status, kSiteBwdQFull, abort_flag);
+        for (int n = 0; ok && n < n_kt; ++n) {
+          const int s = n % C::STAGES;
+          if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull, abort_flag))) break;
+          // S(n) = Q K_n^T into S buffer n & 1, once the elementwise warps have read S(n-2) from it.
+          if (n >= 2 && !(ok = mbar_wait(s_free + (n & 1), ((n >> 1) - 1) & 1, a.status, kSiteBwdSFull, abort_flag)))
             break;
           tc_fence_after_sync();
-          issue_s(n + 1);
-        }
-        const uint32_t k_addr = smem_u32(sK + s * C::TILE_BYTES);
+          const uint32_t dst = tmem + ((n & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull))) break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+            umma_ss_w(dst, q_lo + off, kHi, k_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full + (n & 1));
+          // dP(n) = dO V_n^T overwrites dS(n-1) (read by dQ(n-1)).
+          if (n > 0 && !(ok = mbar_wait(dq_done, (n - 1) & 1, a.status, kSiteBwdDqDone, abort_flag))) break;
           tc_fence_after_sync();
 #pragma unroll
-          for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
-            umma_ts(tmem + C::T_DQ, tmem + C::T_DP + bwd_packed_col(kk),
-                    smem_desc_sw128(k_addr + kk * 16 * 128, C::BLOCK_BYTES, 1024), idesc_ts,
-                    (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+            umma_ss_w(tmem + C::T_DP, do_lo + off, kHi, v_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(dp_full);
+          umma_commit(empty + s);  // this issuer's reads of the stage
         }
-        if (!ok) break;
-        umma_commit(dq_done);
-        umma_commit(empty + s);
+      } else {
+        const uint32_t km_lo = sw128_desc_lo(smem_u32(sK), C::BLOCK_BYTES);  // MN-major K: steps of 16 keys
+        for (int n = 0; ok && n < n_kt; ++n) {
+          const int s = n % C::STAGES;
+          // dQ += dS K, one half of the keys as soon as its warpgroup wrote dS.
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull, abort_flag))) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
+              umma_ts_w(tmem + C::T_DQ, tmem + C::T_DP + bwd_packed_col(kk), km_lo + s * kTileW + kk * (16 * 128 >> 4),
+                        kHi, idesc_ts, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          umma_commit(dq_done);
+          umma_commit(empty + s);  // this issuer's reads of the stage
+        }
+        umma_commit(acc_done);
       }
       if (!ok) *abort_flag = 1;
-      umma_commit(acc_done);
+      // Every MMA either issuer started has finished before TMEM is released
+      // (the barrier completes once both have committed).
       umma_commit(drain);
       mbar_wait(drain, 0, a.status, kSiteBwdDrain);
     }
@@ -703,6 +725,9 @@ __global__ void __launch_bounds__(320, 1)
           p[c + 1] = p1;
         }
       }
+      // S(n) is in registers: its buffer may take S(n+2)
+      tc_fence_before_sync();
+      mbar_arrive(s_free + (n & 1));
       // ---- phase 2: dS = P (dP - Dl), packed over this half's first 32 columns of dP
       if (!(ok = mbar_wait(dp_full, n & 1, a.status, kSiteBwdDpFull))) break;
       tc_fence_after_sync();
