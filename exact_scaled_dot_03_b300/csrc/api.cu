@@ -329,7 +329,8 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   bwd_prep_kernel<D><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
                                             static_cast<const __nv_bfloat16*>(dout), lse, ws, ws + rows, seed_l,
                                             seed_d, scale, heads, Nq, Nq_pad);
-  attn_bwd_dkdv_kernel<D><<<dim3(Hkv, (Nk + 127) / 128, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+  attn_bwd_dkdv_kernel<D><<<dim3(2 * ((Nk + 127) / 128), (Hkv + 1) / 2, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(
+      tq, tk, tv, tdo, a);
   attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -627,7 +628,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
     return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (B > 65535 || (Nq + 127) / 128 > 65535 || (Nk + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || (Nq + 127) / 128 > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y / z limits
   int Nq_pad;
   size_t need;
   if (!plan_bwd(B, Hq, Nq, &Nq_pad, &need)) return ATTN_ERR_INVALID_ARG;

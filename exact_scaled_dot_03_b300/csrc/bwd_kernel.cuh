@@ -252,8 +252,13 @@ __global__ void __launch_bounds__(352, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hkv = blockIdx.x;
-  const int kt = blockIdx.y;  // key tile 0 (most query tiles under causal masking) launches first
+  // Launch order: KV heads in pairs, and within a pair key tile 0 (the most
+  // query tiles under causal masking) first, alternating between the two
+  // heads. The CTAs running at once then share two heads' Q and dO in L2
+  // instead of streaming every head's, and the heaviest tiles still go first.
+  const int kt = blockIdx.x >> 1;
+  const int hkv = 2 * blockIdx.y + (blockIdx.x & 1);
+  if (hkv >= a.Hkv) return;  // odd head count: the last pair has one head (before any setup)
   const int b = blockIdx.z;
   const int key0 = kt * 128;
   // Query tiles holding a row that sees some key of this tile: [qt0, n_qt).

@@ -183,7 +183,8 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
  *               aligned, contents irrelevant (overwritten)
  * Rows of dq that see no key are 0; keys no query sees get dk = dv = 0.
  * scale, causal (bottom-right aligned when Nq != Nk), d and the alignment
- * rules as attn_fwd. Three kernels run on `stream` in order: a per-row
+ * rules as attn_fwd; ceil(Nq / 128), B and Hkv <= 65535, else
+ * ATTN_ERR_UNSUPPORTED. Three kernels run on `stream` in order: a per-row
  * prologue, then dK/dV, then dQ.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

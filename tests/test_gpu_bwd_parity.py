@@ -42,6 +42,7 @@ SMALL = [
     Prefill("bwd_n129", B=1, Hq=2, Hkv=2, Nq=129, Nk=129, d=128, causal=True, seed=38),
     Prefill("bwd_mha_d128_n1024", B=1, Hq=2, Hkv=2, Nq=1024, Nk=1024, d=128, causal=False, seed=39),
     Prefill("bwd_causal_gqa8_n1000", B=1, Hq=16, Hkv=2, Nq=1000, Nk=1000, d=128, causal=True, seed=40),
+    Prefill("bwd_gqa_hkv3_n300", B=2, Hq=6, Hkv=3, Nq=300, Nk=300, d=128, causal=True, seed=43),
 ]
 
 
