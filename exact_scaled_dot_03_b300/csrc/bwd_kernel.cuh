@@ -35,8 +35,8 @@
 // the column values split into three bf16 parts) seeds S^T with -lse/scale and
 // dP^T with -Dl, so the elementwise warps load no per-column value:
 //   dK/dV step: S^T | dP^T (P phase) | dV (dS phase) | dK
-//   dQ step:    dP(n) (P phase) | S(n+1) (dS phase) | dQ(n)
-// (S double-buffered in the dQ kernel so the next one is already queued).
+//   dQ step:    S(n+1) (as soon as S(n) is in registers) | dP(n+1) (while dS(n) and dQ(n) run) | dQ(n)
+// (dP double-buffered in the dQ kernel, so dP(n+1) waits only for dQ(n-1)).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -99,13 +99,13 @@ struct BwdCfg {
   static constexpr int Q_K_OFF = 2 * TILE_BYTES;
   static constexpr int Q_V_OFF = Q_K_OFF + STAGES * TILE_BYTES;
   static constexpr int Q_BAR_OFF = Q_V_OFF + STAGES * TILE_BYTES;
-  // q_full, full[S], empty[S], s_full[2] (one per S buffer), dp_full, ds_full[2], dq_done, acc_done, drain,
-  // s_free[2] (one per S buffer)
-  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 11;
+  // q_full, full[S], empty[S], s_full, s_free, dp_full[2] (per dP buffer), ds_full[2][2] (per dP
+  // buffer and warpgroup), dq_done[2] (per dP buffer), acc_done, drain
+  static constexpr int Q_NUM_BARS = 1 + 2 * STAGES + 13;
   static constexpr int Q_MISC_OFF = Q_BAR_OFF + Q_NUM_BARS * 8;
   static constexpr int Q_SMEM_BYTES = Q_MISC_OFF + 16 + 1024;
-  // TMEM columns: S buffer 0, dP (dS written back over it), dQ, S buffer 1.
-  static constexpr uint32_t T_S0 = 0, T_DP = 128, T_DQ = 256, T_S1 = 384;
+  // TMEM columns: S, dP buffer 0 (dS written back over it), dQ, dP buffer 1.
+  static constexpr uint32_t T_S = 0, T_DP0 = 128, T_DQ = 256, T_DP1 = 384;
 };
 
 // Wait sites recorded in status[1] by the backward kernels.
@@ -536,13 +536,13 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* q_full = bars;
   uint64_t* full = bars + 1;
   uint64_t* empty = full + C::STAGES;
-  uint64_t* s_full = empty + C::STAGES;  // [2], one per S buffer
-  uint64_t* dp_full = s_full + 2;
-  uint64_t* ds_full = dp_full + 1;       // [2] warpgroup g wrote dS of its half
-  uint64_t* dq_done = ds_full + 2;
-  uint64_t* acc_done = dq_done + 1;
+  uint64_t* s_full = empty + C::STAGES;
+  uint64_t* s_free = s_full + 1;         // the elementwise warps read S into registers
+  uint64_t* dp_full = s_free + 1;        // [2] per dP buffer
+  uint64_t* ds_full = dp_full + 2;       // [2][2] dP buffer b, warpgroup g wrote dS of its half: 2b + g
+  uint64_t* dq_done = ds_full + 4;       // [2] per dP buffer
+  uint64_t* acc_done = dq_done + 2;
   uint64_t* drain = acc_done + 1;
-  uint64_t* s_free = drain + 1;          // [2] the elementwise warps read S buffer b into registers
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::Q_MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::Q_MISC_OFF + 4);
 
@@ -566,15 +566,15 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(empty + s, 2);  // released by both MMA issuers
     }
     mbar_init(s_full, 1);
-    mbar_init(s_full + 1, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
-    mbar_init(ds_full + 1, 128);
-    mbar_init(dq_done, 1);
+    mbar_init(s_free, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(dp_full + i, 1);
+      mbar_init(ds_full + 2 * i, 128);
+      mbar_init(ds_full + 2 * i + 1, 128);
+      mbar_init(dq_done + i, 1);
+    }
     mbar_init(acc_done, 1);
     mbar_init(drain, 2);  // one commit from each MMA issuer
-    mbar_init(s_free, 256);
-    mbar_init(s_free + 1, 256);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -633,47 +633,52 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ), 16), do_lo = sw128_desc_lo(smem_u32(sDO), 16);
         const uint32_t k_lo = sw128_desc_lo(smem_u32(sK), 16), v_lo = sw128_desc_lo(smem_u32(sV), 16);
         ok = mbar_wait(q_full, 0, a.status, kSiteBwdQFull, abort_flag);
+        // Every wait below is on a barrier that cannot run two phases ahead of
+        // the one waited for (parity waits cannot tell those apart): S(n+1)
+        // needs s_free(n), dP(n+2) needs dQ(n) through dq_done of its buffer.
         for (int n = 0; ok && n < n_kt; ++n) {
           const int s = n % C::STAGES;
           if (!(ok = mbar_wait(full + s, (n / C::STAGES) & 1, a.status, kSiteBwdFull, abort_flag))) break;
-          // S(n) = Q K_n^T into S buffer n & 1, once the elementwise warps have read S(n-2) from it.
-          if (n >= 2 && !(ok = mbar_wait(s_free + (n & 1), ((n >> 1) - 1) & 1, a.status, kSiteBwdSFull, abort_flag)))
+          // S(n) = Q K_n^T, once the elementwise warps have read S(n-1) into registers.
+          if (n >= 1 && !(ok = mbar_wait(s_free, (n - 1) & 1, a.status, kSiteBwdSFull, abort_flag))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
+            umma_ss_w(tmem + C::T_S, q_lo + off, kHi, k_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+          // dP(n) = dO V_n^T into dP buffer n & 1, which held dS(n-2) (read by dQ(n-2)).
+          if (n >= 2 && !(ok = mbar_wait(dq_done + (n & 1), ((n >> 1) - 1) & 1, a.status, kSiteBwdDqDone, abort_flag)))
             break;
           tc_fence_after_sync();
-          const uint32_t dst = tmem + ((n & 1) ? C::T_S1 : C::T_S0);
+          const uint32_t dst = tmem + ((n & 1) ? C::T_DP1 : C::T_DP0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
-            umma_ss_w(dst, q_lo + off, kHi, k_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
+            umma_ss_w(dst, do_lo + off, kHi, v_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
           }
-          umma_commit(s_full + (n & 1));
-          // dP(n) = dO V_n^T overwrites dS(n-1) (read by dQ(n-1)).
-          if (n > 0 && !(ok = mbar_wait(dq_done, (n - 1) & 1, a.status, kSiteBwdDqDone, abort_flag))) break;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4);
-            umma_ss_w(tmem + C::T_DP, do_lo + off, kHi, v_lo + s * kTileW + off, kHi, idesc_ss, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(dp_full);
+          umma_commit(dp_full + (n & 1));
           umma_commit(empty + s);  // this issuer's reads of the stage
         }
       } else {
         const uint32_t km_lo = sw128_desc_lo(smem_u32(sK), C::BLOCK_BYTES);  // MN-major K: steps of 16 keys
         for (int n = 0; ok && n < n_kt; ++n) {
           const int s = n % C::STAGES;
-          // dQ += dS K, one half of the keys as soon as its warpgroup wrote dS.
+          // dQ += dS K, one half of the keys as soon as its warpgroup wrote dS
+          // (dS(n) sits in dP buffer n & 1).
+          const uint32_t dp = tmem + ((n & 1) ? C::T_DP1 : C::T_DP0);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
-            if (!(ok = mbar_wait(ds_full + g, n & 1, a.status, kSiteBwdDsFull, abort_flag))) break;
+            if (!(ok = mbar_wait(ds_full + 2 * (n & 1) + g, (n >> 1) & 1, a.status, kSiteBwdDsFull, abort_flag))) break;
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 4 * g; kk < 4 * g + 4; ++kk)
-              umma_ts_w(tmem + C::T_DQ, tmem + C::T_DP + bwd_packed_col(kk), km_lo + s * kTileW + kk * (16 * 128 >> 4),
-                        kHi, idesc_ts, (n > 0 || kk > 0) ? 1u : 0u);
+              umma_ts_w(tmem + C::T_DQ, dp + bwd_packed_col(kk), km_lo + s * kTileW + kk * (16 * 128 >> 4), kHi,
+                        idesc_ts, (n > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
-          umma_commit(dq_done);
+          umma_commit(dq_done + (n & 1));
           umma_commit(empty + s);  // this issuer's reads of the stage
         }
         umma_commit(acc_done);
@@ -691,7 +696,7 @@ __global__ void __launch_bounds__(352, 1)
     const int r = wq * 32 + lane;
     const int qi = q0 + r;  // < Nq_pad
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tDP = tmem + lane_off + C::T_DP + 64 * g;
+
     const float sl2 = a.scale_log2;
     const float lse2 = a.lse2[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
     const float dl = a.dl[(size_t)(b * a.Hq + h) * a.Nq_pad + qi];
@@ -702,9 +707,10 @@ __global__ void __launch_bounds__(352, 1)
     const long long lim_first = a.causal ? min((long long)a.Nk - 1, (long long)q0 + a.causal_offset) : a.Nk - 1;
     bool ok = true;
     for (int n = 0; ok && n < n_kt; ++n) {
-      if (!(ok = mbar_wait(s_full + (n & 1), (n >> 1) & 1, a.status, kSiteBwdSFull))) break;
+      if (!(ok = mbar_wait(s_full, n & 1, a.status, kSiteBwdSFull))) break;
       tc_fence_after_sync();
-      const uint32_t tS = tmem + lane_off + ((n & 1) ? C::T_S1 : C::T_S0) + 64 * g;
+      const uint32_t tS = tmem + lane_off + C::T_S + 64 * g;
+      const uint32_t tDP = tmem + lane_off + ((n & 1) ? C::T_DP1 : C::T_DP0) + 64 * g;
       const int kbase = n * 128 + 64 * g;
       const bool need_mask = kbase + 63 > lim_first;
       const int cmax = lim - kbase;  // column c is visible iff c <= cmax
@@ -730,11 +736,11 @@ __global__ void __launch_bounds__(352, 1)
           p[c + 1] = p1;
         }
       }
-      // S(n) is in registers: its buffer may take S(n+2)
+      // S(n) is in registers: the S issuer may compute S(n+1) into its columns
       tc_fence_before_sync();
-      mbar_arrive(s_free + (n & 1));
+      mbar_arrive(s_free);
       // ---- phase 2: dS = P (dP - Dl), packed over this half's first 32 columns of dP
-      if (!(ok = mbar_wait(dp_full, n & 1, a.status, kSiteBwdDpFull))) break;
+      if (!(ok = mbar_wait(dp_full + (n & 1), (n >> 1) & 1, a.status, kSiteBwdDpFull))) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
@@ -754,7 +760,7 @@ __global__ void __launch_bounds__(352, 1)
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(ds_full + g);
+      mbar_arrive(ds_full + 2 * (n & 1) + g);
     }
     if (!ok) *abort_flag = 1;
     // ---------------------------------------------------------- epilogue
