@@ -210,16 +210,20 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
                           const DecodePlan& plan, cudaStream_t stream, int dev, const DecodePaging& pg) {
   static DevFlags smem_set;
   using C = DecCfg<D, GC>;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tk16, tv16;  // 16-row boxes: the partial last tile of a contiguous cache
   if (pg.block_table == nullptr) {
     if (!make_map(&tk, kc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK) ||
-        !make_map(&tv, vc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK))
+        !make_map(&tv, vc, D, Lmax, static_cast<long long>(B) * Hkv, C::TK) ||
+        !make_map(&tk16, kc, D, Lmax, static_cast<long long>(B) * Hkv, 16) ||
+        !make_map(&tv16, vc, D, Lmax, static_cast<long long>(B) * Hkv, 16))
       return ATTN_ERR_CUDA;
   } else {
     const int rows = pg.page_size < C::TK ? pg.page_size : C::TK;
     if (!make_map(&tk, kc, D, pg.page_size, static_cast<long long>(pg.num_pages) * Hkv, rows) ||
         !make_map(&tv, vc, D, pg.page_size, static_cast<long long>(pg.num_pages) * Hkv, rows))
       return ATTN_ERR_CUDA;
+    tk16 = tk;  // unused by the paged path
+    tv16 = tv;
   }
   if (!ensure_smem(attn_decode_kernel<D, GC>, C::SMEM_BYTES, dev, smem_set)) return ATTN_ERR_CUDA;
   DecArgs a;
@@ -253,7 +257,7 @@ attn_status launch_decode(const void* q, const void* kc, const void* vc, const i
   static_assert(C::TK == kDecTile && C::MIN_CHUNK == kDecMinChunk, "decode plan and kernel disagree");
   const int grid = sm_count(dev);  // persistent: one CTA per SM
   if (grid == 0) return ATTN_ERR_CUDA;
-  attn_decode_kernel<D, GC><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, a);
+  attn_decode_kernel<D, GC><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, tk16, tv16, a);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

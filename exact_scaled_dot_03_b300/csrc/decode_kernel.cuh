@@ -180,6 +180,7 @@ __device__ __forceinline__ void dec_advance(const DecArgs& a, int UPB, TileCurso
 template <int D, int GC>
 __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_v16,
                        const DecArgs a) {
   using C = DecCfg<D, GC>;
   extern __shared__ uint8_t smem_raw[];
@@ -295,19 +296,35 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
   };
   // Loads tile c into stage s (warp-collective: lane 0 arms the barrier, the
   // lanes of the page pieces issue their copies).
+  // Contiguous cache: the last tile of a unit is fetched only as far as the
+  // length needs, in 16-row boxes (lane i copies rows [16 i, 16 i + 16)); the
+  // rows past the length are masked (K) and zeroed (V) before use, whatever
+  // the stage held.
   auto issue = [&](const TileCursor& c, int pg, int s) {
     uint8_t* kdst = ring + s * C::STAGE_BYTES;
     uint8_t* vdst = kdst + C::TILE_BYTES;
     const int hkv = c.r / a.qgroups;
-    if (lane == 0) mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+    int rows16 = C::TK;  // rows copied
+    if (a.block_table == nullptr) rows16 = min(C::TK, (dec_len(a, c.b) - c.j * C::TK + 15) & ~15);
+    if (lane == 0) mbar_arrive_expect_tx(full + s, rows16 == C::TK ? C::STAGE_BYTES : 2 * C::KBLK * rows16 * 128);
     __syncwarp();
     if (a.block_table == nullptr) {
-      if (lane == 0) {
-        const int plane = c.b * a.Hkv + hkv;
+      const int plane = c.b * a.Hkv + hkv;
+      if (rows16 == C::TK) {
+        if (lane == 0) {
+#pragma unroll
+          for (int kb = 0; kb < C::KBLK; ++kb) {
+            tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, c.j * C::TK, plane);
+            tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, c.j * C::TK, plane);
+          }
+        }
+      } else if (lane < rows16 / 16) {
 #pragma unroll
         for (int kb = 0; kb < C::KBLK; ++kb) {
-          tma_load_3d(kdst + kb * C::BOX_BYTES, &tm_k, full + s, kb * 64, c.j * C::TK, plane);
-          tma_load_3d(vdst + kb * C::BOX_BYTES, &tm_v, full + s, kb * 64, c.j * C::TK, plane);
+          tma_load_3d(kdst + kb * C::BOX_BYTES + lane * 16 * 128, &tm_k16, full + s, kb * 64, c.j * C::TK + 16 * lane,
+                      plane);
+          tma_load_3d(vdst + kb * C::BOX_BYTES + lane * 16 * 128, &tm_v16, full + s, kb * 64, c.j * C::TK + 16 * lane,
+                      plane);
         }
       }
     } else if (lane < nsub) {
@@ -330,6 +347,8 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
       if (k == 0 && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_k16);
+        tma_prefetch_desc(&tm_v16);
       }
       issue(ahead, lookup_page(ahead), k);
     }
