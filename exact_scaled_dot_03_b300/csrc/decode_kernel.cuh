@@ -585,31 +585,30 @@ __global__ void __launch_bounds__(DecCfg<D, GC>::THREADS, 1)
       pend_b[pend_n] = b;
       pend_h0[pend_n] = h0;
       // A first piece that is not also the last: thread 0 takes its ticket now
-      // (its fence then overlaps the stream); the other pieces of that unit were
-      // started by the previous CTA, so it is rarely the last to arrive.
+      // (its round trip then overlaps the stream); the other pieces of that
+      // unit were started by the previous CTA, so it is rarely the last to
+      // arrive. The barrier above ordered every thread's partial writes before
+      // the ticket, a release; when it is the last, the ticket also acquires
+      // the other pieces' partials.
       pend_early[pend_n] = it_tile < n_tiles;
-      if (pend_early[pend_n] && tid == 0) {
-        __threadfence();
-        pend_last[pend_n] = live && atomicAdd(a.tickets + u_idx, 1) == pieces - 1;
-      }
+      if (pend_early[pend_n] && tid == 0)
+        pend_last[pend_n] = live && atom_add_acq_rel_gpu(a.tickets + u_idx, 1) == pieces - 1;
       ++pend_n;
     }
   }
 
   // ---- settle the partial pieces: the last piece of a unit to finish merges.
   if (pend_n > 0) {
-    __syncthreads();  // every thread's partial writes precede thread 0's fence
+    __syncthreads();  // every thread's partial writes precede thread 0's tickets (releases)
     if (tid == 0) {
       const bool live = !*abort_flag;
-      __threadfence();
       for (int k = 0; k < pend_n; ++k)
         last_flag[k] = pend_early[k] ? pend_last[k]
-                                     : live && atomicAdd(a.tickets + pend_u[k], 1) == pend_pieces[k] - 1;
+                                     : live && atom_add_acq_rel_gpu(a.tickets + pend_u[k], 1) == pend_pieces[k] - 1;
     }
-    __syncthreads();
+    __syncthreads();  // a last ticket (an acquire) precedes every thread's reads of the partials
     for (int k = 0; k < pend_n; ++k) {
       if (!last_flag[k]) continue;
-      __threadfence();
       const int pieces = pend_pieces[k];
       const float* plse = a.part_lse + (size_t)pend_u[k] * a.slots * GC;
       const float* po = a.part_o + (size_t)pend_u[k] * a.slots * GC * D;

@@ -93,6 +93,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   return mbar_wait_slow(bar, parity, status, site, abort_flag, limit_ns);
 }
 
+// ---------------------------------------------------------------- global atomics
+// Fetch-and-add at GPU scope with release and acquire semantics: the caller's
+// earlier writes (and those ordered before them, e.g. by a CTA barrier) are
+// visible to whoever later acquires this location, and the writes released
+// by earlier adds are visible to the caller afterwards.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
