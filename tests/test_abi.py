@@ -206,3 +206,32 @@ def test_stall_hook_host_side(lib):
     assert lib.attn_test_arm_stall(-1) == binding.ERR_INVALID_ARG
     assert lib.attn_test_arm_stall(1) == binding.OK
     assert lib.attn_test_arm_stall(0) == binding.OK   # disarmed again
+
+
+def test_fwd_host_workspace_size_and_argument_checks(lib):
+    # per (batch, KV head) group: K and V, twice (two K/V slots); per chunk slot (three):
+    # Q and O of a whole group's query heads and their LSE, each rounded up to 256 bytes
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    B, Hq, Hkv, Nq, Nk, d = 1, 8, 2, 100, 300, 64
+    G = Hq // Hkv
+    want = 2 * 2 * a256(Nk * d * 2) + 3 * (2 * a256(G * Nq * d * 2) + a256(G * Nq * 4))
+    assert lib.attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d) == want
+    assert lib.attn_fwd_host_workspace_size(B, 6, 4, Nq, Nk, d) == 0      # Hq % Hkv != 0
+    assert lib.attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, 96) == 0  # unsupported d
+    ws = 0x100000
+    f = lambda **kw: lib.attn_fwd_host(*[kw.get(n, dflt) for n, dflt in [  # noqa: E731
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("o", FAKE), ("lse", None), ("B", B), ("Hq", Hq), ("Hkv", Hkv),
+        ("Nq", Nq), ("Nk", Nk), ("d", d), ("scale", 0.125), ("causal", 1), ("ws", ws), ("wsb", want),
+        ("stream", None)]])
+    assert f(q=None) == binding.ERR_INVALID_ARG
+    assert f(o=None) == binding.ERR_INVALID_ARG
+    assert f(k=None) == binding.ERR_INVALID_ARG
+    assert f(Hq=3) == binding.ERR_INVALID_ARG
+    assert f(causal=2) == binding.ERR_INVALID_ARG
+    assert f(scale=0.0) == binding.ERR_INVALID_ARG
+    assert f(ws=None) == binding.ERR_INVALID_ARG
+    assert f(ws=ws + 16) == binding.ERR_INVALID_ARG      # not 256-byte aligned
+    assert f(wsb=want - 1) == binding.ERR_INVALID_ARG
+    assert f(d=96) == binding.ERR_UNSUPPORTED
+    # no queries: nothing to do (q and o may then be NULL), nothing queued
+    assert f(Nq=0, q=None, o=None, wsb=lib.attn_fwd_host_workspace_size(B, Hq, Hkv, 0, Nk, d)) == binding.OK
