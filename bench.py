@@ -24,7 +24,9 @@ Prints one JSON line.
 causal); every other part has its own block with its own roofline (decode:
 GB/s of the cache rows actually read, sum(seqlens)*Hkv*d*2*2 bytes, plus q, o
 and lse). Each roofline gives the fraction of the measured peak and of the
-nominal B300 peak. Under torchrun every rank runs the same workload
+nominal B300 peak. The decode block also carries, as context, the rate of a
+plain device copy moving the same number of bytes, timed after the timed
+region the same way. Under torchrun every rank runs the same workload
 (replicas; weak scaling) and rank 0 prints the aggregate over the
 max-over-ranks time.
 
@@ -443,6 +445,28 @@ def run_ours(args, w, wd):
 
     tot = max_over_ranks({name: sum(v) for name, v in ms.items()}, dev)
     peaks = measured_peaks()
+    copy_ctx = None
+    if do_dec:
+        # Context for the decode's roofline, outside the timed region: a plain
+        # device copy moving the same number of bytes (half read, half written).
+        nb = int(sl_h.sum()) * wd.Hkv * wd.d * 2 * 2 + 2 * wd.B * wd.Hq * wd.d * 2 + 4 * wd.B * wd.Hq
+        src = torch.empty(nb // 2, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        cts = []
+        for r in range(args.warmup + args.steps):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if r >= args.warmup:
+                cts.append(e0.elapsed_time(e1))
+        cms = statistics.median(cts)
+        copy_ctx = {"value": 2 * (nb // 2) / (cms / 1e3) / 1e9, "unit": "GB/s", "ms": cms,
+                    "what": "torch copy_ of half the decode's bytes into a second buffer (the same bytes moved), "
+                            "L2 flushed, median; context for the decode's roofline fraction, not a peak"}
+        del src, dst
     mean_s = lambda name: statistics.mean(ms[name]) / 1e3  # noqa: E731  (seconds per launch)
 
     blocks = {}  # name -> block, in the order they are printed
@@ -464,7 +488,8 @@ def run_ours(args, w, wd):
             "ms": tot["decode"] / args.steps,
             "roofline": hbm_roof(dec_bytes / mean_s("decode") / 1e9, peaks, dec_bytes, "attn_decode_kernel<128,4>",
                                  profiled_traffic("attn_decode_kernel_gqa_traffic.txt",
-                                                  ("decode_kernel.cuh", "ptx.cuh")))}
+                                                  ("decode_kernel.cuh", "ptx.cuh"))),
+            "device_copy_same_bytes": copy_ctx}
     for name, wx in extra:
         f = wx.flops()
         blk = {"metric": f"{'causal ' if wx.causal else ''}prefill TFLOP/s", "workload": wx.name,
