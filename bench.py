@@ -573,6 +573,8 @@ def run_ours(args, w, wd):
         }
         if head_name == "prefill":
             line["prefill_ms"] = headline["ms"]
+        if headline.get("device_copy_same_bytes") is not None:
+            line["device_copy_same_bytes"] = headline["device_copy_same_bytes"]
         # Short blocks first (the five workloads), the longer ones after.
         line.update(blocks)
         line.update({"cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
