@@ -270,16 +270,17 @@ def round_to_bf16(x):
     return out
 
 
-def attention_forward_rope(q, k, v, scale: float, causal: bool, base: float = 10000.0, window: int = 0):
+def attention_forward_rope(q, k, v, scale: float, causal: bool, base: float = 10000.0, window: int = 0, rows=None):
     """Prefill with RoPE applied to Q and K first ([PW] §5.3: it acts on Q
     and K, not on the input). Key j sits at position j and query i at
     position i + (Nk - Nq), the same alignment as the causal rule. The
     rotated Q and K are rounded to bf16 (the inputs' type) before the scores,
-    then the plain definition (attention_forward) is applied."""
+    then the plain definition (attention_forward) is applied, on the query
+    rows ``rows`` only when given (as there)."""
     Nq, Nk = q.shape[-2], k.shape[-2]
     qr = round_to_bf16(rope_rotate(q, np.arange(Nq) + (Nk - Nq), base))
     kr = round_to_bf16(rope_rotate(k, np.arange(Nk), base))
-    return attention_forward(qr, kr, v, scale, causal, window=window)
+    return attention_forward(qr, kr, v, scale, causal, rows=rows, window=window)
 
 
 def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale: float, k_new=None, v_new=None):
