@@ -287,6 +287,34 @@ bool plan_bwd(int B, int Hq, int Nq, int* Nq_pad, size_t* bytes) {
   return true;
 }
 
+// The dQ kernel runs beside the dK/dV kernel on a library stream of lower
+// priority (they share no output): the dK/dV launch keeps the SMs it needs
+// for its heaviest key tiles, and dQ CTAs take up SMs as its last wave thins
+// out. Created once per device; the mutex keeps each call's fork and join
+// (record, wait, launch, record, wait) in one piece when host threads call at
+// once.
+struct BwdPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s_dq = nullptr;
+  cudaEvent_t prep_done = nullptr, dq_done = nullptr;
+};
+BwdPipe& bwd_pipe(int dev) {
+  static BwdPipe pipes[kMaxDevices];
+  return pipes[dev];
+}
+bool bwd_pipe_init(BwdPipe& p) {
+  if (p.ready) return true;
+  int lowest = 0, highest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&lowest, &highest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&p.s_dq, cudaStreamNonBlocking, lowest) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p.prep_done, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p.dq_done, cudaEventDisableTiming) != cudaSuccess)
+    return false;
+  p.ready = true;
+  return true;
+}
+
 template <int D>
 attn_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
@@ -333,10 +361,17 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   bwd_prep_kernel<D><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
                                             static_cast<const __nv_bfloat16*>(dout), lse, ws, ws + rows, seed_l,
                                             seed_d, scale, heads, Nq, Nq_pad);
+  BwdPipe& P = bwd_pipe(dev);
+  std::lock_guard<std::mutex> lock(P.mu);
+  if (!bwd_pipe_init(P)) return ATTN_ERR_CUDA;
+  bool ok = cudaEventRecord(P.prep_done, s) == cudaSuccess;  // both kernels read what the prep kernel wrote
   attn_bwd_dkdv_kernel<D><<<dim3(2 * ((Nk + 127) / 128), (Hkv + 1) / 2, B), C::THREADS, C::KV_SMEM_BYTES, s>>>(
       tq, tk, tv, tdo, a);
-  attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  ok = ok && cudaStreamWaitEvent(P.s_dq, P.prep_done, 0) == cudaSuccess;
+  if (ok) attn_bwd_dq_kernel<D><<<dim3(Hq, (Nq + 127) / 128, B), C::THREADS, C::Q_SMEM_BYTES, P.s_dq>>>(tq, tk, tv, tdo, a);
+  ok = ok && cudaEventRecord(P.dq_done, P.s_dq) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(s, P.dq_done, 0) == cudaSuccess;  // the call ends on `stream` with both
+  return ok && cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 }  // namespace
 

@@ -184,8 +184,12 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
  * Rows of dq that see no key are 0; keys no query sees get dk = dv = 0.
  * scale, causal (bottom-right aligned when Nq != Nk), d and the alignment
  * rules as attn_fwd; ceil(Nq / 128), B and Hkv <= 65535, else
- * ATTN_ERR_UNSUPPORTED. Three kernels run on `stream` in order: a per-row
- * prologue, then dK/dV, then dQ.
+ * ATTN_ERR_UNSUPPORTED. Three kernels: a per-row prologue on `stream`, then
+ * dK/dV on `stream` and dQ beside it on a library stream of lower priority
+ * (created once per device). `stream` waits for dQ through an event, so work
+ * queued on `stream` after the call sees all three gradients, as if every
+ * kernel had run on it. Calls from several host threads enqueue one at a
+ * time.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,

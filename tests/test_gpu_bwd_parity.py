@@ -186,3 +186,28 @@ def test_causal_gqa_16384_sampled():
     samples = [(0, 3, np.sort(rng.choice(w.Nq, 48, replace=False))),
                (0, 60, np.concatenate([np.arange(4), np.arange(w.Nq - 4, w.Nq)]))]
     _full_size(w, samples, key_check)
+
+
+def test_calls_on_two_streams_back_to_back():
+    """Two backward calls queued on two streams before any synchronisation share
+    the library's dQ stream and events: each must return the bits it returns
+    when run alone."""
+    wa = Prefill("bwd_stream_a", B=1, Hq=4, Hkv=2, Nq=640, Nk=640, d=128, causal=True, seed=44)
+    wb = Prefill("bwd_stream_b", B=2, Hq=2, Hkv=1, Nq=300, Nk=500, d=64, causal=True, seed=45)
+    cases = []
+    for w in (wa, wb):
+        q, k, v, do = (t.to(DEV) for t in backward_inputs(w))
+        o, lse = binding.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        alone = binding.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        cases.append((w, (q, k, v, o, lse, do), [t.clone() for t in alone]))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results = []
+    for (w, (q, k, v, o, lse, do), _), st in zip(cases, streams):
+        with torch.cuda.stream(st):
+            results.append(binding.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale))
+    torch.cuda.synchronize()
+    assert binding.device_status()[0] == binding.OK
+    for (w, _, alone), got in zip(cases, results):
+        for name, a, g in zip(("dq", "dk", "dv"), alone, got):
+            assert torch.equal(a, g), f"{w.name} {name}"
