@@ -355,6 +355,7 @@ attn_status launch_bwd(const void* q, const void* k, const void* v, const void* 
   a.status = status_ptr(dev);
   const int sms = sm_count(dev);
   if (a.status == nullptr || sms == 0) return ATTN_ERR_CUDA;
+  a.stall = take_stall(ATTN_TEST_STALL_BACKWARD);
   const long long heads = static_cast<long long>(B) * Hq;
   const long long threads = heads * Nq_pad * (D / 8);
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
@@ -820,7 +821,9 @@ uint64_t attn_kv_cache_bytes(int64_t layers, int64_t n, int64_t h_kv, int64_t d_
 const char* attn_version(void) { return "exact-attn-sm103 0.1"; }
 
 attn_status attn_test_arm_stall(int kind) {
-  if (kind != 0 && kind != ATTN_TEST_STALL_PREFILL && kind != ATTN_TEST_STALL_DECODE) return ATTN_ERR_INVALID_ARG;
+  if (kind != 0 && kind != ATTN_TEST_STALL_PREFILL && kind != ATTN_TEST_STALL_DECODE &&
+      kind != ATTN_TEST_STALL_BACKWARD)
+    return ATTN_ERR_INVALID_ARG;
   g_armed_stall.store(kind);
   return ATTN_OK;
 }

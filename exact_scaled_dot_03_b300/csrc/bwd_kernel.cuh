@@ -64,6 +64,10 @@ struct BwdArgs {
   float scale;         // applied to dQ and dK in the epilogues
   float scale_log2;    // scale * log2(e)
   unsigned* status;
+  // Failure-detection test hook: when set, the elementwise warpgroup 0 of the
+  // dK/dV kernel's block (0, 0, 0) replaces its first score wait by a wait on
+  // a barrier that nothing arrives on, with a 1 ms limit (0 in normal use).
+  int stall;
 };
 
 template <int D>
@@ -85,8 +89,8 @@ struct BwdCfg {
   static constexpr int KV_SEED_OFF = KV_DO_OFF + STAGES * TILE_BYTES;      // per stage: -lse seed, -Dl seed
   static constexpr int KV_ONES_OFF = KV_SEED_OFF + STAGES * 2 * SEED_BYTES;  // 128 x 16: ones in columns 0-2
   static constexpr int KV_BAR_OFF = KV_ONES_OFF + SEED_BYTES;
-  // kv_full, full[S], empty[S], s_full, dp_full, p_full[2], ds_full[2], dv_done, dk_done, acc_done, drain
-  static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 10;
+  // kv_full, full[S], empty[S], s_full, dp_full, p_full[2], ds_full[2], dv_done, dk_done, acc_done, drain, stall
+  static constexpr int KV_NUM_BARS = 1 + 2 * STAGES + 11;
   static constexpr int KV_MISC_OFF = KV_BAR_OFF + KV_NUM_BARS * 8;
   static constexpr int KV_SMEM_BYTES = KV_MISC_OFF + 16 + 1024;
   // TMEM columns: S^T, dP^T (128 each; P^T and dS^T are written back over
@@ -247,6 +251,7 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* dk_done = dv_done + 1;
   uint64_t* acc_done = dk_done + 1;
   uint64_t* drain = acc_done + 1;
+  uint64_t* stall_bar = drain + 1;  // test hook only: never arrived on
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::KV_MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::KV_MISC_OFF + 4);
 
@@ -287,6 +292,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(dk_done, 1);
     mbar_init(acc_done, 1);
     mbar_init(drain, 2);  // one commit from each MMA issuer
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -436,6 +442,15 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tST = tmem + lane_off + C::T_ST + 64 * g, tDPT = tmem + lane_off + C::T_DPT + 64 * g;
     const float sl2 = a.scale_log2;
     bool ok = true;
+    if (a.stall != 0 && g == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && n_steps > 0) {
+      // test hook: in place of its first score wait, warpgroup 0 of block (0, 0, 0)
+      // waits on a barrier nothing arrives on; it gives up after 1 ms and takes the
+      // abort path. The backward's elementwise and copy waits do not watch the abort
+      // flag (that keeps their polling light), so the other roles of the CTA give up
+      // at their own limit; the status keeps the first site.
+      mbar_wait(stall_bar, 0, a.status, kSiteBwdSFull, abort_flag, kStallLimitNs);
+      ok = false;
+    }
     for (int n = 0; ok && n < n_steps; ++n) {
       const int s = n % C::STAGES;
       const int q0 = (qt0 + n % per_head) * 128;

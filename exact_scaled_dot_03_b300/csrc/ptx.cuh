@@ -64,8 +64,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Slow path of a bounded wait: spin on try_wait. Gives up after `limit_ns`:
 // ORs kStatusWaitTimeout into status[0], records the call site and block in
-// status[1..2] and returns false. If `abort_flag` is given, it also returns
-// false (recording nothing) as soon as another role of the CTA has set that
+// status[1..2] if no wait had given up before, and returns false. If
+// `abort_flag` is given, it also returns false (recording nothing) as soon
+// as another role of the CTA has set that
 // flag, so one give-up ends the whole CTA's pipeline within microseconds.
 // Waits that let in-flight copies or MMAs land before the CTA exits pass no
 // flag: they must run to completion.
@@ -76,9 +77,12 @@ __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, u
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
-      atomicOr(status, kStatusWaitTimeout);
-      atomicExch(status + 1, site);
-      atomicExch(status + 2, blockIdx.x + 65536u * blockIdx.y);
+      // the first wait to give up records its site and block (the cause; later
+      // give-ups in the same launch follow from it)
+      if ((atomicOr(status, kStatusWaitTimeout) & kStatusWaitTimeout) == 0) {
+        atomicExch(status + 1, site);
+        atomicExch(status + 2, blockIdx.x + 65536u * blockIdx.y);
+      }
       return false;
     }
   }

@@ -335,10 +335,13 @@ ATTN_API attn_status attn_decode_noalloc(const void* q, const void* k_cache, con
  * a hang.
  *
  * Every internal wait of the kernels is bounded (1 s). When one gives up, the
- * kernel records ATTN_ERR_TIMEOUT, the wait site and the block in the status
- * word, every other role of that CTA stops waiting, the copies and MMAs still
- * in flight are allowed to land, tensor memory is freed and the kernel
- * returns; attn_device_status() then reports it.
+ * kernel records ATTN_ERR_TIMEOUT and, for the first wait of the launch to give
+ * up, its site and block in the status word. The other roles of that CTA stop
+ * waiting: at once in the prefill and decode, and in the backward at their own
+ * limit (its elementwise and copy waits do not watch for an abort, which keeps
+ * their polling light). The copies and MMAs still in flight are allowed to
+ * land, tensor memory is freed and the kernel returns; attn_device_status()
+ * then reports it.
  *
  * attn_test_arm_stall(kind) arms the next launch, in this process, of one
  * kernel: in its first CTA one role waits on a barrier that nothing ever
@@ -347,6 +350,9 @@ ATTN_API attn_status attn_decode_noalloc(const void* q, const void* k_cache, con
  *                            query tile 0, first score tile (wait site 8)
  *   ATTN_TEST_STALL_DECODE   attn_decode / _paged / _noalloc: warp 0, first
  *                            K/V tile (wait site 20)
+ *   ATTN_TEST_STALL_BACKWARD attn_bwd (a call with queries and keys): the dK/dV
+ *                            kernel's elementwise warps of query columns
+ *                            0-63, first score tile (wait site 38)
  * The hook disarms itself at that launch; kind 0 disarms it. The outputs of
  * the stalled launch are undefined, and a decode workspace it used must be
  * zero-filled again before reuse (its tickets are left part-counted). Returns
@@ -354,6 +360,7 @@ ATTN_API attn_status attn_decode_noalloc(const void* q, const void* k_cache, con
  */
 #define ATTN_TEST_STALL_PREFILL 1
 #define ATTN_TEST_STALL_DECODE 2
+#define ATTN_TEST_STALL_BACKWARD 3
 ATTN_API attn_status attn_test_arm_stall(int kind);
 
 /* Library version string, e.g. "exact-attn-sm103 0.1". */

@@ -204,6 +204,8 @@ def test_stall_hook_host_side(lib):
     disarms it); nothing is launched here."""
     assert lib.attn_test_arm_stall(7) == binding.ERR_INVALID_ARG
     assert lib.attn_test_arm_stall(-1) == binding.ERR_INVALID_ARG
+    assert lib.attn_test_arm_stall(4) == binding.ERR_INVALID_ARG
+    assert lib.attn_test_arm_stall(3) == binding.OK   # the backward's kind
     assert lib.attn_test_arm_stall(1) == binding.OK
     assert lib.attn_test_arm_stall(0) == binding.OK   # disarmed again
 

@@ -1,7 +1,7 @@
 """The give-up path of the kernels' bounded waits, exercised on the GPU
 without a fault or a hang.
 
-Every internal wait of the prefill and decode kernels is bounded. The library's
+Every internal wait of the prefill, decode and backward kernels is bounded. The library's
 test hook (attn_test_arm_stall) makes one role of the first CTA of the next
 launch wait on a barrier that nothing arrives on, with a 1 ms limit. That wait
 gives up, the kernel takes its normal abort path: the other roles of the CTA
@@ -19,14 +19,15 @@ import torch
 
 import oracle
 from exact_scaled_dot_03_b300 import binding
-from exact_scaled_dot_03_b300.workloads import Decode, Prefill, decode_inputs, prefill_inputs
-from tests.parity import compare, f64
+from exact_scaled_dot_03_b300.workloads import Decode, Prefill, backward_inputs, decode_inputs, prefill_inputs
+from tests.parity import compare, compare_grad, f64
 
 pytestmark = pytest.mark.gpu
 
-STALL_PREFILL, STALL_DECODE = 1, 2   # ATTN_TEST_STALL_* in include/attn.h
+STALL_PREFILL, STALL_DECODE, STALL_BACKWARD = 1, 2, 3   # ATTN_TEST_STALL_* in include/attn.h
 SITE_PREFILL_S_FULL = 8              # the prefill softmax warps' score wait
 SITE_DECODE_FULL = 20                # the decode warps' K/V tile wait
+SITE_BACKWARD_S_FULL = 38            # the dK/dV kernel's elementwise score wait
 
 
 def _stalled(call, kind):
@@ -70,6 +71,28 @@ def test_decode_wait_gives_up_and_the_next_call_is_exact():
     assert binding.device_status()[0] == binding.OK
     o_ref, lse_ref = oracle.attention_decode(f64(q), f64(kc), f64(vc), sl.cpu().numpy(), w.scale)
     print(compare(o, lse, o_ref, lse_ref, "after the stalled decode"))
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_backward_wait_gives_up_and_the_next_call_is_exact(d):
+    w = Prefill("timeout_backward", B=1, Hq=4, Hkv=2, Nq=700, Nk=700, d=d, causal=True, seed=80 + d)
+    q, k, v, do = (t.cuda() for t in backward_inputs(w))
+    o, lse = binding.fwd(q, k, v, causal=True, scale=w.scale)
+    code, detail, secs = _stalled(lambda: binding.bwd(q, k, v, o, lse, do, causal=True, scale=w.scale),
+                                  STALL_BACKWARD)
+    assert code == binding.ERR_TIMEOUT, (code, detail)
+    assert detail[1] == SITE_BACKWARD_S_FULL and detail[2] == 0, detail
+    # the backward's elementwise and copy waits do not watch the abort flag: the
+    # CTA's other roles give up at their own 1 s limit (all at about the same time)
+    assert secs < 3.0, f"abort took {secs:.3f} s"
+    # the hook disarmed itself: the next call runs normally and is exact
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert binding.device_status()[0] == binding.OK
+    *ref, m = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), w.scale, True, magnitudes=True)
+    for name, g, r, t, sd in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (m["tq"], m["tk"], m["tv"]),
+                                 (m["sq"], m["sk"], None)):
+        compare_grad(g, r, t, sd, f"after the stalled backward: {name}")
 
 
 def test_disarmed_hook_changes_nothing():
