@@ -521,6 +521,19 @@ def test_rope_is_a_pairwise_rotation():
     np.testing.assert_allclose(rope_rotate(v, [1], base=b)[0, 2:], [-5.0, 3.0], atol=1e-12)
 
 
+@pytest.mark.parametrize("Nq,Nk,window", [(40, 40, 0), (30, 45, 0), (40, 40, 7)])
+def test_rope_row_subset_is_exact(Nq, Nk, window):
+    """Asking for a subset of query rows gives those rows of the full result
+    (the rows keep their positions: the rotation uses each row's own position)."""
+    rng = np.random.default_rng(11)
+    q, k, v = _rand(rng, 1, 2, Nq, 8), _rand(rng, 1, 1, Nk, 8), _rand(rng, 1, 1, Nk, 8)
+    o, lse = attention_forward_rope(q, k, v, 0.3, True, base=100.0, window=window)
+    rows = np.array([0, 1, Nq // 2, Nq - 1])
+    o2, lse2 = attention_forward_rope(q, k, v, 0.3, True, base=100.0, window=window, rows=rows)
+    np.testing.assert_allclose(o2, o[:, :, rows], atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[:, :, rows], atol=1e-13)
+
+
 def test_rope_attention_matches_rotating_by_hand_and_rounding():
     rng = np.random.default_rng(72)
     B, Hq, Hkv, Nq, Nk, d = 1, 4, 2, 9, 13, 8
